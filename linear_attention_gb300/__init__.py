@@ -3,13 +3,14 @@
 The compute runs in hand-written sm_103a CUDA kernels behind a C-ABI shared library
 (``include/based.h``); ``linear_attention_gb300.based`` is a thin ctypes binding to it.
 """
+import importlib
+
 __all__ = ["based_fwd", "based_fwd_host"]
 
 
 def __getattr__(name):
     # The binding is imported lazily so that the input generators can be used without the
     # CUDA library being built.
-    if name in ("based_fwd", "based_fwd_host", "based"):
-        from . import based
-        return based if name == "based" else getattr(based, name)
+    if name in ("based_fwd", "based_fwd_host"):
+        return getattr(importlib.import_module(".based", __name__), name)
     raise AttributeError(name)

@@ -1,0 +1,370 @@
+// based_fwd.cu: C ABI of the Based causal forward pass (declared in include/based.h).
+//
+// Host side: argument checks, the work partition, tensor maps, the library-owned workspace and
+// the launch sequence  [aggregate -> scan] -> forward  on the caller's stream. All arithmetic of
+// the method runs in the kernels of based_kernels.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/based.h"
+#include "based_kernels.cuh"
+
+namespace {
+
+using namespace based;
+
+thread_local char tl_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char *what) {
+    snprintf(tl_cuda_error, sizeof(tl_cuda_error), "%s: %s", what, cudaGetErrorString(e));
+    return BASED_ERR_CUDA;
+}
+#define BASED_CUDA(call)                                   \
+    do {                                                   \
+        cudaError_t e_ = (call);                           \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (no link-time libcuda dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// (dim0, H, T, B) bf16 tensor with a (box0, 1, 128, 1) box.
+int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, int box0,
+             CUtensorMapSwizzle swz) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) {
+        snprintf(tl_cuda_error, sizeof(tl_cuda_error), "cuTensorMapEncodeTiled unavailable");
+        return BASED_ERR_CUDA;
+    }
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d0) * 2,
+                                   static_cast<cuuint64_t>(H) * d0 * 2,
+                                   static_cast<cuuint64_t>(T) * H * d0 * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), 1, static_cast<cuuint32_t>(kChunk), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(tl_cuda_error, sizeof(tl_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
+                 static_cast<int>(r));
+        return BASED_ERR_CUDA;
+    }
+    return BASED_OK;
+}
+
+struct Plan {
+    int n_c;        // chunks per head
+    long long N;    // chunks in total
+    int G;          // CTAs
+    bool need_agg;  // some range ends inside a head
+    int slot_floats;
+    size_t ws_bytes;
+};
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    std::mutex m;
+    bool init = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    bool attrs_done[2][2] = {{false, false}, {false, false}};
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    void *hbuf = nullptr;  // based_fwd_host staging (q | k | v | o)
+    size_t hbuf_bytes = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int *dev) {
+    BASED_CUDA(cudaGetDevice(dev));
+    if (*dev < 0 || *dev >= kMaxDevices) return BASED_ERR_NO_DEVICE;
+    DeviceState &d = g_dev[*dev];
+    std::lock_guard<std::mutex> lk(d.m);
+    if (!d.init) {
+        cudaDeviceProp prop;
+        BASED_CUDA(cudaGetDeviceProperties(&prop, *dev));
+        d.sms = prop.multiProcessorCount;
+        d.cc_major = prop.major;
+        d.cc_minor = prop.minor;
+        d.init = true;
+    }
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return BASED_ERR_NO_DEVICE;
+    return BASED_OK;
+}
+
+int slot_floats(int K, int V) { return (V + 1) * ((K == 16) ? 160 : 48); }
+
+Plan make_plan(int B, int T, int H, int K, int V, int sms) {
+    Plan p;
+    p.n_c = (T + kChunk - 1) / kChunk;
+    p.N = static_cast<long long>(B) * H * p.n_c;
+    p.G = static_cast<int>(p.N < sms ? p.N : sms);
+    p.need_agg = false;
+    for (int i = 0; i < p.G; ++i)
+        if (has_aggregate(p.N, p.G, i, p.n_c)) p.need_agg = true;
+    p.slot_floats = slot_floats(K, V);
+    p.ws_bytes = p.need_agg ? static_cast<size_t>(p.G) * p.slot_floats * sizeof(float) : 0;
+    return p;
+}
+
+int check_args(const void *q, const void *k, const void *v, int B, int T, int H, int K, int V,
+               const void *o) {
+    if (!q || !k || !v || !o) return BASED_ERR_NULL_POINTER;
+    if (K != 8 && K != 16) return BASED_ERR_UNSUPPORTED_K;
+    if (V != 64 && V != 128) return BASED_ERR_UNSUPPORTED_V;
+    if (B < 1 || T < 1 || H < 1) return BASED_ERR_BAD_SHAPE;
+    if (static_cast<long long>(B) * T * H >= (1ll << 31)) return BASED_ERR_BAD_SHAPE;
+    auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(q) || !al(k) || !al(v) || !al(o)) return BASED_ERR_MISALIGNED;
+    const size_t rows = static_cast<size_t>(B) * T * H;
+    auto overlap = [](const void *a, size_t na, const void *b, size_t nb) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return x < y + nb && y < x + na;
+    };
+    const size_t ob = rows * V * 4;
+    if (overlap(o, ob, q, rows * K * 2) || overlap(o, ob, k, rows * K * 2) ||
+        overlap(o, ob, v, rows * V * 2))
+        return BASED_ERR_ALIASING;
+    return BASED_OK;
+}
+
+template <int K, int V>
+int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
+           float scale, float *o, float *ws, const Plan &p, DeviceState &d, cudaStream_t st,
+           cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+    using CF = Cfg<K, V>;
+    {
+        std::lock_guard<std::mutex> lk(d.m);
+        bool &done = d.attrs_done[K == 16][V == 128];
+        if (!done) {
+            BASED_CUDA(cudaFuncSetAttribute(based_fwd_kernel<K, V>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_FWD));
+            BASED_CUDA(cudaFuncSetAttribute(based_agg_kernel<K, V>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_AGG));
+            done = true;
+        }
+    }
+    CUtensorMap mq, mk, mv;
+    int rc;
+    const CUtensorMapSwizzle sw_qk = CU_TENSOR_MAP_SWIZZLE_32B;
+    if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
+    if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
+    if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != BASED_OK) return rc;
+    if (p.need_agg) {
+        based_agg_kernel<K, V><<<p.G, kAggThreads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.N, p.G);
+        BASED_CUDA(cudaGetLastError());
+        dim3 grid((p.slot_floats + 255) / 256, p.G);
+        based_scan_kernel<<<grid, 256, 0, st>>>(ws, p.slot_floats, p.n_c, p.N, p.G);
+        BASED_CUDA(cudaGetLastError());
+    }
+    if (ev_begin) BASED_CUDA(cudaEventRecord(ev_begin, st));
+    based_fwd_kernel<K, V><<<p.G, kFwdThreads, CF::SMEM_FWD, st>>>(mq, mk, mv, o, ws, T, H, p.n_c,
+                                                                      p.N, p.G, scale);
+    BASED_CUDA(cudaGetLastError());
+    if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
+    return BASED_OK;
+}
+
+int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H, int K, int V,
+        float scale, float *o, void *ws, size_t ws_bytes, bool own_ws, based_stream_t stream,
+        void *ev_begin = nullptr, void *ev_end = nullptr) {
+    int rc = check_args(q, k, v, B, T, H, K, V, o);
+    if (rc != BASED_OK) return rc;
+    int dev;
+    if ((rc = current_device(&dev)) != BASED_OK) return rc;
+    DeviceState &d = g_dev[dev];
+    const Plan p = make_plan(B, T, H, K, V, d.sms);
+    if (!(scale > 0.0f) || std::isnan(scale)) scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
+    if (own_ws) {
+        std::lock_guard<std::mutex> lk(d.m);
+        if (p.ws_bytes > d.ws_bytes) {
+            if (d.ws) {
+                cudaError_t e = cudaFree(d.ws);
+                d.ws = nullptr;
+                d.ws_bytes = 0;
+                if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+            }
+            BASED_CUDA(cudaMalloc(&d.ws, p.ws_bytes));
+            d.ws_bytes = p.ws_bytes;
+        }
+        ws = d.ws;
+        ws_bytes = d.ws_bytes;
+    } else if (p.ws_bytes > 0) {
+        if (!ws || ws_bytes < p.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 15u))
+            return BASED_ERR_WORKSPACE;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *w = static_cast<float *>(ws);
+    cudaEvent_t eb = static_cast<cudaEvent_t>(ev_begin), ee = static_cast<cudaEvent_t>(ev_end);
+    if (K == 16 && V == 64) return launch<16, 64>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    if (K == 16 && V == 128) return launch<16, 128>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    if (K == 8 && V == 64) return launch<8, 64>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    return launch<8, 128>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+}
+
+}  // namespace
+
+extern "C" {
+
+int based_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H, int K,
+              int V, float scale, float *o, based_stream_t stream) {
+    return run(q, k, v, B, T, H, K, V, scale, o, nullptr, 0, true, stream);
+}
+
+int based_fwd_timed(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
+                    int K, int V, float scale, float *o, based_stream_t stream, void *ev_begin,
+                    void *ev_end) {
+    return run(q, k, v, B, T, H, K, V, scale, o, nullptr, 0, true, stream, ev_begin, ev_end);
+}
+
+int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
+    if ((K != 8 && K != 16) || (V != 64 && V != 128) || B < 1 || T < 1 || H < 1) return 0;
+    int dev;
+    if (current_device(&dev) != BASED_OK) return 0;
+    return make_plan(B, T, H, K, V, g_dev[dev].sms).need_agg ? 3 : 1;
+}
+
+size_t based_fwd_workspace_size(int B, int T, int H, int K, int V) {
+    if ((K != 8 && K != 16) || (V != 64 && V != 128) || B < 1 || T < 1 || H < 1) return 0;
+    int dev;
+    if (current_device(&dev) != BASED_OK) return 0;
+    return make_plan(B, T, H, K, V, g_dev[dev].sms).ws_bytes;
+}
+
+int based_fwd_ws(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
+                 int K, int V, float scale, float *o, void *workspace, size_t ws_bytes,
+                 based_stream_t stream) {
+    return run(q, k, v, B, T, H, K, V, scale, o, workspace, ws_bytes, false, stream);
+}
+
+int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_t *v_host, int B,
+                   int T, int H, int K, int V, float scale, float *o_host, based_stream_t stream) {
+    if (!q_host || !k_host || !v_host || !o_host) return BASED_ERR_NULL_POINTER;
+    if (K != 8 && K != 16) return BASED_ERR_UNSUPPORTED_K;
+    if (V != 64 && V != 128) return BASED_ERR_UNSUPPORTED_V;
+    if (B < 1 || T < 1 || H < 1 || static_cast<long long>(B) * T * H >= (1ll << 31))
+        return BASED_ERR_BAD_SHAPE;
+    int dev, rc;
+    if ((rc = current_device(&dev)) != BASED_OK) return rc;
+    DeviceState &d = g_dev[dev];
+    const size_t rows = static_cast<size_t>(B) * T * H;
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t bq = up(rows * K * 2), bv = up(rows * V * 2), bo = up(rows * V * 4);
+    const size_t need = 2 * bq + bv + bo;
+    uint8_t *base;
+    {
+        std::lock_guard<std::mutex> lk(d.m);
+        if (need > d.hbuf_bytes) {
+            if (d.hbuf) {
+                cudaError_t e = cudaFree(d.hbuf);
+                d.hbuf = nullptr;
+                d.hbuf_bytes = 0;
+                if (e != cudaSuccess) return cuda_fail(e, "cudaFree(staging)");
+            }
+            BASED_CUDA(cudaMalloc(&d.hbuf, need));
+            d.hbuf_bytes = need;
+        }
+        base = static_cast<uint8_t *>(d.hbuf);
+    }
+    uint16_t *dq = reinterpret_cast<uint16_t *>(base);
+    uint16_t *dk = reinterpret_cast<uint16_t *>(base + bq);
+    uint16_t *dv = reinterpret_cast<uint16_t *>(base + 2 * bq);
+    float *dout = reinterpret_cast<float *>(base + 2 * bq + bv);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    BASED_CUDA(cudaMemcpyAsync(dq, q_host, rows * K * 2, cudaMemcpyHostToDevice, st));
+    BASED_CUDA(cudaMemcpyAsync(dk, k_host, rows * K * 2, cudaMemcpyHostToDevice, st));
+    BASED_CUDA(cudaMemcpyAsync(dv, v_host, rows * V * 2, cudaMemcpyHostToDevice, st));
+    rc = based_fwd(dq, dk, dv, B, T, H, K, V, scale, dout, stream);
+    if (rc != BASED_OK) return rc;
+    BASED_CUDA(cudaMemcpyAsync(o_host, dout, rows * V * 4, cudaMemcpyDeviceToHost, st));
+    BASED_CUDA(cudaStreamSynchronize(st));
+    return BASED_OK;
+}
+
+int based_device_status(int device, unsigned int *status, int clear) {
+    if (!status) return BASED_ERR_NULL_POINTER;
+    int prev;
+    BASED_CUDA(cudaGetDevice(&prev));
+    if (device != prev) BASED_CUDA(cudaSetDevice(device));
+    cudaError_t e = cudaMemcpyFromSymbol(status, based::g_status, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(based::g_status, &zero, sizeof(unsigned int));
+    }
+    if (device != prev) cudaSetDevice(prev);
+    if (e != cudaSuccess) return cuda_fail(e, "status word");
+    return BASED_OK;
+}
+
+int based_selftest_wait_timeout(unsigned long long limit_ns) {
+    if (limit_ns < 1000ull) limit_ns = 1000ull;
+    if (limit_ns > 2000000000ull) limit_ns = 2000000000ull;
+    int dev;
+    BASED_CUDA(cudaGetDevice(&dev));
+    unsigned int before;
+    int rc = based_device_status(dev, &before, 1);
+    if (rc != BASED_OK) return rc;
+    int *res = nullptr;
+    BASED_CUDA(cudaMalloc(&res, sizeof(int)));
+    based::based_selftest_wait_kernel<<<1, 1>>>(limit_ns, res);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int h = -1;
+    if (e == cudaSuccess) e = cudaMemcpy(&h, res, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(res);
+    if (e != cudaSuccess) return cuda_fail(e, "selftest kernel");
+    unsigned int st;
+    rc = based_device_status(dev, &st, 1);
+    if (rc != BASED_OK) return rc;
+    // the wait must have given up (result 0) and recorded site 255
+    if (h != 0 || (st & 1u) == 0u || ((st >> 8) & 0xFFu) != 255u) return BASED_ERR_BAD_ARGUMENT;
+    return BASED_OK;
+}
+
+const char *based_strerror(int code) {
+    switch (code) {
+        case BASED_OK: return "ok";
+        case BASED_ERR_NULL_POINTER: return "null pointer";
+        case BASED_ERR_UNSUPPORTED_K: return "unsupported K (must be 8 or 16)";
+        case BASED_ERR_UNSUPPORTED_V: return "unsupported V (must be 64 or 128)";
+        case BASED_ERR_BAD_SHAPE: return "bad shape (B, T, H >= 1 and B*T*H < 2^31)";
+        case BASED_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case BASED_ERR_ALIASING: return "output overlaps an input";
+        case BASED_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case BASED_ERR_CUDA: return "CUDA error";
+        case BASED_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+        case BASED_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
+        case BASED_ERR_BAD_ARGUMENT: return "invalid argument";
+        default: return "unknown error code";
+    }
+}
+
+const char *based_last_cuda_error(void) { return tl_cuda_error; }
+
+int based_abi_version(void) { return 10000; }
+
+}  // extern "C"

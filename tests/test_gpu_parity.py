@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the same seeded
+bf16 inputs.
+
+Bar (the Based forward workload definition): max|o_gpu - o_oracle| <= 2e-2 and
+mean|o_gpu - o_oracle| <= 2e-3 in fp32 output units; the relative Frobenius error against the
+spec's correctness gate (2e-2) is asserted too. Small cases compare every output; the full-size
+workloads compare every row of sampled heads (the chunked oracle computes a head exactly, in
+fp64, in seconds).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_gb300.based import (BasedError, based_fwd, based_fwd_host, device_status,
+                                          selftest_wait_timeout, workspace_size)
+from linear_attention_gb300.inputs import WORKLOADS, make_inputs, make_workload
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, REL_FRO = 2e-2, 2e-3, 2e-2
+
+
+def _errors(o_gpu: np.ndarray, ref: np.ndarray):
+    d = np.abs(o_gpu.astype(np.float64) - ref)
+    return float(d.max()), float(d.mean()), float(np.linalg.norm(d) / np.linalg.norm(ref))
+
+
+def _assert_close(o_gpu, ref, what):
+    mx, mn, rf = _errors(o_gpu, ref)
+    assert np.isfinite(o_gpu).all(), f"{what}: non-finite output"
+    assert mx <= MAX_ABS and mn <= MEAN_ABS and rf <= REL_FRO, (what, mx, mn, rf)
+    return mx, mn, rf
+
+
+def _scale(K, scale):
+    return oracle.default_scale(K) if scale is None else float(np.float32(scale))
+
+
+def _run_gpu(q, k, v, scale, dev):
+    o = based_fwd(q.to(dev), k.to(dev), v.to(dev), scale=scale)
+    torch.cuda.synchronize(dev)
+    return o.cpu().numpy()
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(cuda_device):
+    device_status(0, clear=True)
+    yield
+    assert device_status(0, clear=True) == 0, "a kernel gave up a bounded wait"
+
+
+# ------------------------------------------------------------------------------------------------
+# Small shapes: every output compared. Cover both K, both V, ragged tails, T below one chunk,
+# ranges that split heads anywhere (more chunks than SMs and fewer).
+# ------------------------------------------------------------------------------------------------
+SMALL = [
+    # B, T, H, K, V, seed, scale
+    (1, 1, 1, 16, 64, 10, None),
+    (1, 1, 3, 8, 128, 11, None),
+    (2, 63, 2, 16, 64, 12, None),
+    (1, 64, 2, 8, 64, 13, 0.5),
+    (1, 65, 2, 16, 128, 14, None),
+    (1, 127, 1, 8, 128, 15, None),
+    (1, 128, 2, 16, 64, 16, None),
+    (1, 129, 2, 16, 64, 17, 0.2),
+    (2, 257, 3, 8, 64, 18, None),
+    (1, 384, 2, 16, 128, 19, None),
+    (3, 1000, 5, 16, 64, 20, None),
+    (2, 700, 3, 8, 128, 21, 0.3),
+    (1, 1536, 1, 16, 128, 22, None),
+    (2, 4096, 8, 8, 64, 23, None),
+]
+
+
+@pytest.mark.parametrize("B,T,H,K,V,seed,scale", SMALL,
+                         ids=[f"B{c[0]}T{c[1]}H{c[2]}K{c[3]}V{c[4]}" for c in SMALL])
+def test_small_shapes_match_oracle(B, T, H, K, V, seed, scale, cuda_device):
+    q, k, v = make_inputs(B, T, H, K, V, seed)
+    o = _run_gpu(q, k, v, scale, cuda_device)
+    ref, _ = oracle.chunked(q, k, v, _scale(K, scale), chunk=64)
+    _assert_close(o, ref, (B, T, H, K, V))
+
+
+# ------------------------------------------------------------------------------------------------
+# The five workloads at full size, in the launch configuration the benchmark times.
+# ------------------------------------------------------------------------------------------------
+def _sample_heads(B, H, n):
+    total = B * H
+    if total <= n:
+        return list(range(total))
+    idx = np.linspace(0, total - 1, n).round().astype(int)
+    return sorted(set(int(i) for i in idx))
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_matches_oracle(name, cuda_device):
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    o = _run_gpu(q, k, v, w.scale, cuda_device)
+    sc = _scale(w.K, w.scale)
+    if w.B * w.T * w.H <= 2 * 2048 * 16:  # tiny and mid: every head
+        ref, _ = oracle.chunked(q, k, v, sc, chunk=256)
+        _assert_close(o, ref, name)
+    else:
+        heads = _sample_heads(w.B, w.H, 4 if w.T <= 4096 else 3)
+        ref, _ = oracle.chunked(q, k, v, sc, chunk=256, heads=heads)
+        got = np.stack([o[h // w.H, :, h % w.H, :] for h in heads])
+        _assert_close(got, ref, (name, heads))
+    assert np.isfinite(o).all()
+
+
+def test_long_context_sampled_rows_direct_definition(cuda_device):
+    """Rows at the end of the longest sequence against the O(T^2) definition itself."""
+    w = WORKLOADS["long"]
+    q, k, v = make_workload(w)
+    o = _run_gpu(q, k, v, w.scale, cuda_device)
+    rng = np.random.default_rng(0)
+    pairs = [(int(h), int(t)) for h, t in zip(rng.integers(0, w.B * w.H, 24),
+                                                rng.integers(w.T - 4096, w.T, 24))]
+    pairs += [(0, w.T - 1), (w.H - 1, w.T - 1), (3, 0), (5, 127), (7, 128)]
+    ref, _ = oracle.direct_rows(q, k, v, _scale(w.K, w.scale), pairs)
+    got = np.stack([o[h // w.H, t, h % w.H, :] for h, t in pairs])
+    _assert_close(got, ref, "long rows")
+
+
+# ------------------------------------------------------------------------------------------------
+# Contract checks
+# ------------------------------------------------------------------------------------------------
+def test_inputs_unchanged_and_deterministic(cuda_device):
+    q, k, v = [t.to(cuda_device) for t in make_inputs(2, 777, 4, 16, 64, 30)]
+    qc, kc, vc = q.clone(), k.clone(), v.clone()
+    o1 = based_fwd(q, k, v)
+    o2 = based_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(q, qc) and torch.equal(k, kc) and torch.equal(v, vc)
+    assert torch.equal(o1, o2)
+
+
+def test_default_scale_and_nonpositive_scale(cuda_device):
+    q, k, v = [t.to(cuda_device) for t in make_inputs(1, 300, 2, 8, 64, 31)]
+    o_none = based_fwd(q, k, v, scale=None)
+    o_expl = based_fwd(q, k, v, scale=8 ** -0.5)
+    o_neg = based_fwd(q, k, v, scale=-3.0)
+    torch.cuda.synchronize()
+    assert torch.equal(o_none, o_expl) and torch.equal(o_none, o_neg)
+
+
+def test_caller_workspace_matches_library_workspace(cuda_device):
+    B, T, H, K, V = 2, 3000, 3, 16, 128
+    q, k, v = [t.to(cuda_device) for t in make_inputs(B, T, H, K, V, 32)]
+    nbytes = workspace_size(B, T, H, K, V)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=cuda_device)
+    o1 = based_fwd(q, k, v)
+    o2 = based_fwd(q, k, v, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    with pytest.raises(BasedError):
+        based_fwd(q, k, v, workspace=ws[: nbytes // 2])
+
+
+def test_host_entry_point_matches_device_entry_point(cuda_device):
+    q, k, v = make_inputs(1, 1100, 4, 8, 128, 33)
+    o_dev = _run_gpu(q, k, v, None, cuda_device)
+    o_host = based_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), device=cuda_device)
+    assert np.array_equal(o_dev, o_host.numpy())
+
+
+def test_output_not_written_past_end(cuda_device):
+    B, T, H, K, V = 1, 200, 3, 16, 64
+    q, k, v = [t.to(cuda_device) for t in make_inputs(B, T, H, K, V, 34)]
+    buf = torch.full((B * T * H * V + 4096,), 7.0, dtype=torch.float32, device=cuda_device)
+    out = buf[: B * T * H * V].view(B, T, H, V)
+    based_fwd(q, k, v, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[B * T * H * V:] == 7.0)
+
+
+def test_bounded_wait_reports_timeout_without_hanging(cuda_device):
+    selftest_wait_timeout(20_000_000)  # 20 ms limit; raises if the status path misbehaves
+    q, k, v = [t.to(cuda_device) for t in make_inputs(1, 256, 2, 8, 64, 35)]
+    based_fwd(q, k, v)  # the context is still usable afterwards
+    torch.cuda.synchronize()
