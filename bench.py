@@ -282,11 +282,11 @@ def run_gpu(args, w, world, rank, local):
     torch.cuda.synchronize(dev)
 
     # warm-up: W steps, then keep stepping for at least 1 s so clocks settle under load
-    clocks = ClockSampler(local).start() if rank == 0 else None
+    clocks = ClockSampler(local).start() if (rank == 0 and not args.profile) else None
     for i in range(max(3, args.warmup)):
         based_fwd(*sets[i % nsets][:3], scale=w.scale, out=sets[i % nsets][3])
     torch.cuda.synchronize(dev)
-    t_end = time.time() + 1.0
+    t_end = time.time() + (0.0 if args.profile else 1.0)
     i = 0
     while time.time() < t_end or (clocks is not None and clocks.nsamples() < 3 and
                                   time.time() < t_end + 5):
@@ -328,7 +328,7 @@ def run_gpu(args, w, world, rank, local):
 
     # end-to-end through the host entry point: pinned host inputs -> GPU -> pinned host output
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.profile:
         qh, kh, vh = q0.pin_memory(), k0.pin_memory(), v0.pin_memory()
         oh = torch.empty(B, T, H, V, dtype=torch.float32).pin_memory()
         for _ in range(3):
@@ -346,7 +346,7 @@ def run_gpu(args, w, world, rank, local):
 
     if rank != 0:
         return 0
-    cpu = None if (args.no_cpu_baseline or world > 1) else cpu_baseline(w)
+    cpu = None if (args.no_cpu_baseline or args.profile or world > 1) else cpu_baseline(w)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -379,6 +379,8 @@ def main():
     ap.add_argument("--workload", default="headline", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the W warm-up and K timed steps (for running under ncu)")
     args = ap.parse_args()
     if args.steps < 1:
         ap.error("--steps must be >= 1")

@@ -109,7 +109,8 @@ BASED_API int based_fwd_timed(const uint16_t *q, const uint16_t *k, const uint16
                               void *ev_begin, void *ev_end);
 
 /* Number of kernels one based_fwd call launches for this shape on the current device: 1 (the
- * forward kernel alone) or 3 (aggregate, scan, forward); 0 for an unsupported shape. */
+ * forward kernel alone), 2 (aggregate, forward: no range continues another's prefix) or 3
+ * (aggregate, scan, forward); 0 for an unsupported shape. */
 BASED_API int based_fwd_kernel_count(int B, int T, int H, int K, int V);
 
 /* Reads (and, if clear != 0, resets) the device status word of `device`: 0 means no kernel of

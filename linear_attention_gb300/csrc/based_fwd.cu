@@ -50,9 +50,9 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// (dim0, H, T, B) bf16 tensor with a (box0, 1, 128, 1) box.
+// (dim0, H, T, B) tensor of 2-byte (bf16) or 4-byte (fp32) elements with a (box0, 1, 128, 1) box.
 int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, int box0,
-             CUtensorMapSwizzle swz) {
+             CUtensorMapSwizzle swz, bool fp32 = false) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) {
         snprintf(tl_cuda_error, sizeof(tl_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -60,12 +60,14 @@ int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, in
     }
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d0) * 2,
-                                   static_cast<cuuint64_t>(H) * d0 * 2,
-                                   static_cast<cuuint64_t>(T) * H * d0 * 2};
+    const cuuint64_t es = fp32 ? 4 : 2;
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d0) * es,
+                                   static_cast<cuuint64_t>(H) * d0 * es,
+                                   static_cast<cuuint64_t>(T) * H * d0 * es};
     const cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), 1, static_cast<cuuint32_t>(kChunk), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+    CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -83,6 +85,7 @@ struct Plan {
     bool need_agg;  // some range ends inside a head
     int slot_floats;
     size_t ws_bytes;
+    ScanRuns runs;  // runs of ranges whose partial states chain into one head's prefix
 };
 
 constexpr int kMaxDevices = 64;
@@ -122,10 +125,12 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms) {
     Plan p;
     p.n_c = (T + kChunk - 1) / kChunk;
     p.N = static_cast<long long>(B) * H * p.n_c;
-    p.G = static_cast<int>(p.N < sms ? p.N : sms);
+    const int gmax = sms < kMaxRanges ? sms : kMaxRanges;
+    p.G = static_cast<int>(p.N < gmax ? p.N : gmax);
     p.need_agg = false;
     for (int i = 0; i < p.G; ++i)
         if (has_aggregate(p.N, p.G, i, p.n_c)) p.need_agg = true;
+    p.runs = make_scan_runs(p.N, p.G, p.n_c);
     p.slot_floats = slot_floats(K, V);
     p.ws_bytes = p.need_agg ? static_cast<size_t>(p.G) * p.slot_floats * sizeof(float) : 0;
     return p;
@@ -168,21 +173,24 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
             done = true;
         }
     }
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     int rc;
     const CUtensorMapSwizzle sw_qk = CU_TENSOR_MAP_SWIZZLE_32B;
     if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != BASED_OK) return rc;
+    if ((rc = make_map(&mo, o, V, B, T, H, 32, CU_TENSOR_MAP_SWIZZLE_128B, true)) != BASED_OK) return rc;
     if (p.need_agg) {
         based_agg_kernel<K, V><<<p.G, kAggThreads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.N, p.G);
         BASED_CUDA(cudaGetLastError());
-        dim3 grid((p.slot_floats + 255) / 256, p.G);
-        based_scan_kernel<<<grid, 256, 0, st>>>(ws, p.slot_floats, p.n_c, p.N, p.G);
-        BASED_CUDA(cudaGetLastError());
+        if (p.runs.n > 0) {
+            dim3 grid((p.slot_floats / 4 + 255) / 256, p.runs.n);
+            based_scan_kernel<<<grid, 256, 0, st>>>(ws, p.slot_floats, p.runs);
+            BASED_CUDA(cudaGetLastError());
+        }
     }
     if (ev_begin) BASED_CUDA(cudaEventRecord(ev_begin, st));
-    based_fwd_kernel<K, V><<<p.G, kFwdThreads, CF::SMEM_FWD, st>>>(mq, mk, mv, o, ws, T, H, p.n_c,
+    based_fwd_kernel<K, V><<<p.G, kFwdThreads, CF::SMEM_FWD, st>>>(mq, mk, mv, mo, ws, T, H, p.n_c,
                                                                       p.N, p.G, scale);
     BASED_CUDA(cudaGetLastError());
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
@@ -245,7 +253,8 @@ int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
     if ((K != 8 && K != 16) || (V != 64 && V != 128) || B < 1 || T < 1 || H < 1) return 0;
     int dev;
     if (current_device(&dev) != BASED_OK) return 0;
-    return make_plan(B, T, H, K, V, g_dev[dev].sms).need_agg ? 3 : 1;
+    const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms);
+    return p.need_agg ? (p.runs.n > 0 ? 3 : 2) : 1;
 }
 
 size_t based_fwd_workspace_size(int B, int T, int H, int K, int V) {
@@ -366,5 +375,13 @@ const char *based_strerror(int code) {
 const char *based_last_cuda_error(void) { return tl_cuda_error; }
 
 int based_abi_version(void) { return 10000; }
+
+#ifdef BASED_TRACE
+// Trace builds only: device buffer of (CTAs x 64 x 32) uint64 stage timestamps, or NULL to stop.
+__attribute__((visibility("default"))) int based_trace_set(void *buf) {
+    cudaError_t e = cudaMemcpyToSymbol(based::g_trace, &buf, sizeof(void *));
+    return e == cudaSuccess ? 0 : cuda_fail(e, "trace buffer");
+}
+#endif
 
 }  // extern "C"

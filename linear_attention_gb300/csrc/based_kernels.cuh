@@ -2,16 +2,18 @@
 //
 // Method (the "based_forward.py" kernel-task spec, spec_md and perf_md): with the symmetric
 // 2nd-order feature map f(x) (constant, linear, squared and pairwise-product terms, P = 1 + K +
-// K(K+1)/2 features, which reproduces phi(q).phi(k) = 1 + q.k + (q.k)^2/2 exactly once each
-// feature carries its coefficient), every head is cut into chunks of 128 rows and, per chunk c,
-//     s   = q_c k_c^T                      (tensor core, TMEM)
-//     A   = (1 + sigma s + sigma^2 s^2 / 2) masked to j <= i   (fp32 polynomial -> bf16 TMEM)
-//     O   = A v_c + f(q_c) [S | z]         (tensor core; z gives the inter-chunk denominator)
-//     o   = O_num / (rowsum(A) + O_den + 1e-6)
-//     S  += v_c^T f(k_c),  z += f(k_c)^T 1  (tensor core, fp32 accumulation in TMEM)
-// The per-head chunk sequence is split across CTAs; the state each CTA starts from is the sum of
-// the partial states of the chunks before it (aggregate pass + scan), so the forward kernel never
-// waits on another CTA.
+// K(K+1)/2 features; with per-feature coefficients it reproduces phi(q).phi(k) = 1 + q.k +
+// (q.k)^2/2 exactly), every head is cut into chunks of 128 rows and, per chunk c,
+//     s   = q_c k_c^T                              (tensor core -> TMEM, fp32)
+//     A   = 1 + sigma s + sigma^2 s^2 / 2, j <= i   (fp32 polynomial -> bf16 in TMEM)
+//     O   = A [v_c | 1] + f~(q_c) [S | z]          (tensor core; the ones column gives rowsum A,
+//                                                    z gives the inter-chunk denominator)
+//     o   = O_num / (O_den + 1e-6)
+//     S  += v_c^T f(k_c),  z += f(k_c)^T 1         (tensor core, fp32 accumulation in TMEM)
+// where f~(q) = f(sigma q) carries the feature coefficients (1, 1, 1/2 on squares, 1 on cross
+// products). The per-head chunk sequence is split across CTAs; the state each CTA starts from is
+// the sum of the partial states of the chunks before it (aggregate pass + scan), so the forward
+// kernel never waits on another CTA.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -23,16 +25,42 @@ namespace based {
 constexpr int kChunk = 128;            // rows per chunk = MMA M
 constexpr int kFwdThreads = 512;       // 4 warpgroups
 constexpr int kAggThreads = 384;       // 3 warpgroups
+constexpr int kAggStages = 3;          // k/v stages of the aggregate kernel
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after 1 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // drain of in-flight copies after an abort
 
 // Status word: bit 0 = some wait timed out; bits 8..15 = site of the first timeout.
 __device__ unsigned int g_status;
 
+// Optional stage timestamps (clock64) for pipeline analysis, compiled in only with -DBASED_TRACE:
+// g_trace[(cta * 64 + chunk) * 32 + event], chunks >= 64 are not recorded.
+#ifdef BASED_TRACE
+__device__ unsigned long long *g_trace;
+#define BASED_TRACE_INIT unsigned long long *const trace_buf_ = g_trace
+#define BASED_TRACE_EV(n, ev)                                                                 \
+    do {                                                                                      \
+        if (trace_buf_ != nullptr && (n) < 64)                                                \
+            trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + (n)) * 32 + (ev)] = clock64(); \
+    } while (0)
+#else
+#define BASED_TRACE_INIT \
+    do {                 \
+    } while (0)
+#define BASED_TRACE_EV(n, ev) \
+    do {                      \
+    } while (0)
+#endif
+enum TraceEvent {
+    TE_TMA_ISSUE = 0, TE_A_READY, TE_AV_ISSUED, TE_QK_ISSUED, TE_UPD_ISSUED, TE_RO_ISSUED,
+    TE_POLY_BEGIN, TE_POLY_END, TE_PHIK_BEGIN, TE_PHIK_END, TE_PHIQ_BEGIN, TE_PHIQ_END,
+    TE_EPI_BEGIN, TE_EPI_OFREE, TE_EPI_END, TE_CONV_BEGIN, TE_CONV_READ, TE_CONV_END,
+    TE_POLY_LD0, TE_POLY_ST0, TE_POLY_LD1, TE_POLY_ST1
+};
+
 enum WaitSite : uint32_t {
     SITE_STAGE_FREE = 1, SITE_TMA_FULL, SITE_S_FULL, SITE_A_FULL, SITE_O_FULL, SITE_O_FREE,
     SITE_AV_DONE, SITE_PHIQ_FULL, SITE_PHIQ_FREE, SITE_PHIK_FULL, SITE_PHIK_FREE, SITE_UPD_DONE,
-    SITE_SBF_FULL, SITE_AGG_DONE, SITE_DRAIN, SITE_SELFTEST = 255
+    SITE_SBF_FULL, SITE_CONV_READ, SITE_AGG_DONE, SITE_DRAIN, SITE_SELFTEST = 255
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t site) {
@@ -70,19 +98,24 @@ struct Cfg {
     // Feature blocks of 16 features (bf16: one 32-byte row per token per block).
     static constexpr int NBLK = (K == 16) ? 10 : 3;
     static constexpr int PP = NBLK * 16;  // padded feature count (153 -> 160, 45 -> 48)
-    // z rides as row V of S^T when that row exists inside the 128-row MMA (V = 64); otherwise a
-    // separate small MMA accumulates it.
+    // V = 64: z rides as row 64 of S^T, the ones column of [v | 1] is a spare operand block, and
+    // TMEM/SMEM leave room to double-buffer O and the bf16 state operand (pipelined order
+    // AV, QK, UPD, RO). V = 128: a small extra MMA accumulates z; single buffers (order AV, RO,
+    // QK, UPD).
     static constexpr bool ZROW = (V == 64);
-    static constexpr int NO = V + 16;        // O columns: V numerators, den hi, den lo, padding
+    static constexpr bool FAST = (V == 64);
+    static constexpr int NO = V + 16;        // O columns: V numerators, den (rowsum + z_hi), z_lo
     static constexpr int SROWS = V + 1;      // rows of a stored state: V rows of S^T + z
     static constexpr int SLOT = SROWS * PP;  // floats per stored state
 
     // TMEM columns (forward kernel)
-    static constexpr int TM_S = 0;                               // S^T (lanes = value dim)
-    static constexpr int TM_SA = align_up(PP, 32);               // s (fp32) then A (bf16)
-    static constexpr int TM_O = TM_SA + 128;                     // O (lanes = query rows)
-    static constexpr int TM_Z = align_up(TM_O + NO, 32);         // z tiles (V = 128)
-    static_assert(TM_Z + 32 <= 512, "TMEM overflow");
+    static constexpr int TM_S = 0;                                  // S^T (lanes = value dim)
+    static constexpr int TM_SC = align_up(PP, 32);                  // s (fp32 scores)
+    static constexpr int TM_A = FAST ? TM_SC + 128 : TM_SC;         // A (bf16), over s if V=128
+    static constexpr int TM_O0 = FAST ? TM_A + 64 : TM_SC + 128;    // O (lanes = query rows)
+    static constexpr int TM_O1 = FAST ? TM_O0 + NO : TM_O0;
+    static constexpr int TM_Z = align_up(TM_O1 + NO, 32);           // z tiles (V = 128)
+    static_assert(ZROW ? (TM_O1 + NO <= 512) : (TM_Z + 32 <= 512), "TMEM overflow");
     // TMEM columns (aggregate kernel)
     static constexpr int TA_Z = align_up(PP, 32);
     static_assert(TA_Z + 32 <= 256, "TMEM overflow (aggregate)");
@@ -94,30 +127,39 @@ struct Cfg {
     static constexpr int SBF_ROWS = V + 16;    // rows of the bf16 state operand [S | z_hi z_lo 0]
     static constexpr int SBF_BLK = SBF_ROWS * 32;
     static constexpr int SBF = NBLK * SBF_BLK;
+    static constexpr int NSBF = FAST ? 2 : 1;
+    // q/k/v stages in flight: as many as fit (loads are issued NST - 1 chunks ahead)
+    static constexpr int NST = (K == 16 && V == 128) ? 2 : 3;
     static constexpr int OFF_RAWQ = 0;
-    static constexpr int OFF_RAWK = OFF_RAWQ + 2 * RAW;
-    static constexpr int OFF_V = OFF_RAWK + 2 * RAW;
-    static constexpr int OFF_ONES = OFF_V + 2 * VT;
-    static constexpr int OFF_PHIK = OFF_ONES + (ZROW ? VT : 0);
+    static constexpr int OFF_RAWK = OFF_RAWQ + NST * RAW;
+    static constexpr int OFF_V = OFF_RAWK + NST * RAW;
+    // ones block: one 16-token k-step of an MN-major SW128 atom (2 KB), re-used by every k-step
+    static constexpr int ONES = ZROW ? 2048 : 0;
+    static constexpr int OFF_ONES = OFF_V + NST * VT;
+    static constexpr int OFF_PHIK = OFF_ONES + ONES;
     static constexpr int OFF_PHIQ = OFF_PHIK + PHI;
     static constexpr int OFF_SBF = OFF_PHIQ + PHI;
-    static constexpr int OFF_ZONES = align_up(OFF_SBF + SBF, 1024);
-    static constexpr int OFF_BAR = OFF_ZONES + 1024;
+    static constexpr int OFF_ZONES = align_up(OFF_SBF + NSBF * SBF, 1024);
+    // output staging for TMA stores: 128 rows x 32 fp32 (SW128), one quarter/half of a tile
+    static constexpr int OST = kChunk * 128;
+    static constexpr int OFF_OST = OFF_ZONES + 1024;
+    static constexpr int OFF_BAR = OFF_OST + OST;
     static constexpr int SMEM_FWD = OFF_BAR + 256 + 1024;  // + alignment slack
     // The z MMA reads 8 feature blocks (32 KB) from the phi(k) tile start; they must be inside
     // the allocation even when the tile has fewer blocks (their rows of D are never read).
     static_assert(ZROW || OFF_PHIK + 8 * 4096 <= OFF_BAR, "z MMA window leaves shared memory");
     static_assert(SMEM_FWD <= 232448, "shared memory budget");
 
-    // Shared memory (aggregate kernel)
+    // Shared memory (aggregate kernel): two phi(k) buffers, kAggStages k/v stages.
     static constexpr int A_OFF_PHIK = 0;
-    static constexpr int A_OFF_RAWK = align_up(PHI, 1024);
-    static constexpr int A_OFF_V = A_OFF_RAWK + 2 * RAW;
-    static constexpr int A_OFF_ONES = A_OFF_V + 2 * VT;
-    static constexpr int A_OFF_ZONES = A_OFF_ONES + (ZROW ? VT : 0);
+    static constexpr int A_OFF_RAWK = align_up(2 * PHI, 1024);
+    static constexpr int A_OFF_V = A_OFF_RAWK + kAggStages * RAW;
+    static constexpr int A_OFF_ONES = A_OFF_V + kAggStages * VT;
+    static constexpr int A_OFF_ZONES = align_up(A_OFF_ONES + ONES, 1024);
     static constexpr int A_OFF_BAR = A_OFF_ZONES + 1024;
     static constexpr int SMEM_AGG = A_OFF_BAR + 256 + 1024;
-    static_assert(ZROW || A_OFF_PHIK + 8 * 4096 <= A_OFF_BAR, "z MMA window (aggregate)");
+    static_assert(ZROW || A_OFF_PHIK + PHI + 8 * 4096 <= A_OFF_BAR, "z MMA window (aggregate)");
+    static_assert(SMEM_AGG <= 232448, "shared memory budget (aggregate)");
 };
 
 // Swizzled byte offsets inside 32-byte-row (SW32) and 128-byte-row (SW128) tiles whose base is
@@ -127,6 +169,16 @@ __device__ __forceinline__ uint32_t sw32(int row, int half) {
 }
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+// Advance a shared-memory descriptor's start address by `bytes` (stays inside the 14-bit field).
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+// v_c operand at k-step j (16 tokens = 2048 bytes of an MN-major SW128 tile). With a ones block
+// as the second 64-wide atom (LBO measured from the start address), the LBO shrinks as the start
+// advances, so every k-step reads the same 2 KB ones block.
+template <bool ONES_ATOM>
+__device__ __forceinline__ uint64_t v_step(uint64_t d, int j) {
+    const uint64_t step = static_cast<uint64_t>(2048 * j) >> 4;
+    return ONES_ATOM ? d + step - (step << 16) : d + step;
 }
 
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
@@ -138,33 +190,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);
 }
-
-// Coefficient of feature p = 16 f + j of the symmetric feature map (see build_features): the
-// scaled polynomial sigma (q.k) + sigma^2 (q.k)^2 / 2 splits into linear terms (sigma), squares
-// (sigma^2 / 2) and distinct cross products (sigma^2); the constant feature has 1, padding 0.
-template <int K>
-__device__ __forceinline__ float feature_coef(int f, int j, float c_lin, float c_sq, float c_x) {
-    if (K == 16) {
-        if (f == 0) return c_lin;
-        if (f == 1) return c_sq;
-        if (f <= 8) return c_x;
-        return j < 8 ? c_x : (j == 8 ? 1.0f : 0.0f);
-    } else {
-        if (f == 0) return j < 8 ? c_lin : c_sq;
-        if (f == 1) return c_x;
-        return j < 12 ? c_x : (j == 12 ? 1.0f : 0.0f);
-    }
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+// bf16x2 of the Taylor weights 1 + c1 s + c2 s^2 for two fp32 scores, evaluated as
+// fma(s, fma(c2, s, c1), 1) on packed fp32 pairs (square kept in fp32).
+__device__ __forceinline__ uint32_t taylor2(uint32_t s_lo, uint32_t s_hi, uint64_t C2, uint64_t C1,
+                                           uint64_t ONE) {
+    uint32_t out;
+    asm("{\n\t.reg .b64 s2, t2, a2;\n\t.reg .b32 alo, ahi;\n\t"
+        "mov.b64 s2, {%1, %2};\n\t"
+        "fma.rn.f32x2 t2, s2, %3, %4;\n\t"
+        "fma.rn.f32x2 a2, s2, t2, %5;\n\t"
+        "mov.b64 {alo, ahi}, a2;\n\t"
+        "cvt.rn.bf16x2.f32 %0, ahi, alo;\n\t}"
+        : "=r"(out)
+        : "r"(s_lo), "r"(s_hi), "l"(C2), "l"(C1), "l"(ONE));
+    return out;
 }
 
-// Builds the feature tile row of one token from its raw 16-wide bf16 row (SW32 tile) into NBLK
+// Builds one token's row of a feature tile from its raw 16-wide bf16 row (SW32 tile) into NBLK
 // SW32 blocks of 16 features. Products are exact bf16 products rounded once (mul.rn.bf16x2).
 // K = 16: block 0 = x, 1 = x_a^2, 1+d (d = 1..7) = x_a x_{(a+d) mod 16}, 9 = [x_a x_{a+8} (a<8),
 //         1, 0 x 7].
 // K = 8:  block 0 = [x, x_a^2], 1 = [x_a x_{a+1}, x_a x_{a+2}] (mod 8), 2 = [x_a x_{a+3} (mod 8),
 //         x_a x_{a+4} (a<4), 1, 0 x 3].
-// Every unordered pair a < b appears exactly once.
-template <int K>
-__device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t) {
+// Every unordered pair a < b appears exactly once. With SCALED (the query side) the row is
+// f~(x) = f(sigma x) with the squares halved: x is first multiplied by sig2 = (sigma, sigma),
+// so that f~(q).f(k) = 1 + sigma q.k + sigma^2 (q.k)^2 / 2.
+template <int K, bool SCALED>
+__device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t sig2) {
     const uint32_t rb = raw + static_cast<uint32_t>(t) * 32u;
     const uint32_t sw = static_cast<uint32_t>(((t >> 2) & 1) << 4);
     const uint4 lo = ld_shared_v4(rb + sw);
@@ -175,12 +230,17 @@ __device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t
         st_shared_v4(base + (16u ^ sw), p4, p5, p6, p7);
     };
     constexpr uint32_t ONE_ZERO = 0x00003F80u;  // bf16 pair (1.0, 0.0)
+    constexpr uint32_t HALF2 = 0x3F003F00u;     // bf16 pair (0.5, 0.5)
+    auto sq = [&](uint32_t x) { return SCALED ? bmul2(bmul2(x, HALF2), x) : bmul2(x, x); };
     if constexpr (K == 16) {
         const uint4 hi = ld_shared_v4(rb + (16u ^ sw));
-        const uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        if (SCALED) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], sig2);
+        }
         store_blk(0, X[0], X[1], X[2], X[3], X[4], X[5], X[6], X[7]);
-        store_blk(1, bmul2(X[0], X[0]), bmul2(X[1], X[1]), bmul2(X[2], X[2]), bmul2(X[3], X[3]),
-                  bmul2(X[4], X[4]), bmul2(X[5], X[5]), bmul2(X[6], X[6]), bmul2(X[7], X[7]));
+        store_blk(1, sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]), sq(X[4]), sq(X[5]), sq(X[6]), sq(X[7]));
 #pragma unroll
         for (int d = 1; d <= 7; ++d) {
             uint32_t P[8];
@@ -199,9 +259,12 @@ __device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t
         store_blk(9, bmul2(X[0], X[4]), bmul2(X[1], X[5]), bmul2(X[2], X[6]), bmul2(X[3], X[7]),
                   ONE_ZERO, 0u, 0u, 0u);
     } else {
-        const uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
-        store_blk(0, X[0], X[1], X[2], X[3], bmul2(X[0], X[0]), bmul2(X[1], X[1]),
-                  bmul2(X[2], X[2]), bmul2(X[3], X[3]));
+        uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
+        if (SCALED) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], sig2);
+        }
+        store_blk(0, X[0], X[1], X[2], X[3], sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]));
         uint32_t R1[4], R3[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -237,39 +300,58 @@ __host__ __device__ __forceinline__ bool continues_prefix(long long N, int G, in
     return p.g1 > p.g0 && (p.g0 % n_c) != 0 && (p.g0 / n_c) == ((p.g1 - 1) / n_c);
 }
 
-struct ChunkInfo {
-    int b, h, c, t0;
-    bool has_ro, has_upd, upd_acc;
+// Walks the chunks of a range without divisions: (b, h, c) advance like an odometer.
+struct Cursor {
+    int n, last, c, h, b, n_c, H;
+    __device__ __forceinline__ void init(long long g, int nchunks, int n_c_, int H_) {
+        n_c = n_c_;
+        H = H_;
+        n = 0;
+        last = nchunks - 1;
+        const long long head = g / n_c;
+        c = static_cast<int>(g - head * n_c);
+        h = static_cast<int>(head % H);
+        b = static_cast<int>(head / H);
+    }
+    __device__ __forceinline__ void next() {
+        ++n;
+        if (++c == n_c) {
+            c = 0;
+            if (++h == H) {
+                h = 0;
+                ++b;
+            }
+        }
+    }
+    __device__ __forceinline__ int t0() const { return c * kChunk; }
+    // a non-zero state precedes this chunk (inter-chunk read-out needed)
+    __device__ __forceinline__ bool has_ro() const { return c > 0; }
+    // a later chunk of this range continues the head (state update needed)
+    __device__ __forceinline__ bool has_upd() const { return !(n == last || c == n_c - 1); }
+    // the update accumulates onto a carried state
+    __device__ __forceinline__ bool upd_acc() const { return c > 0; }
 };
-__device__ __forceinline__ ChunkInfo chunk_info(long long g, long long g1, int n_c, int H) {
-    ChunkInfo ci;
-    const long long head = g / n_c;
-    ci.c = static_cast<int>(g % n_c);
-    ci.b = static_cast<int>(head / H);
-    ci.h = static_cast<int>(head % H);
-    ci.t0 = ci.c * kChunk;
-    ci.has_ro = ci.c > 0;                                     // a non-zero state precedes
-    ci.has_upd = !((g == g1 - 1) || (ci.c == n_c - 1));       // a later chunk of this range uses it
-    ci.upd_acc = ci.c > 0;                                    // accumulate onto the carried state
-    return ci;
-}
 
 // ------------------------------------------------------------------------------------------------
 // Forward kernel
+// warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle (warp 2 owns TMEM)
+// warps 4-7: Taylor weights A | warps 8-11: feature tiles + output epilogue | warps 12-15: state
+// conversion S^T (fp32 TMEM) -> bf16 operand
 // ------------------------------------------------------------------------------------------------
 enum FwdBar {
-    FB_TMA_FULL0 = 0, FB_TMA_FULL1, FB_STAGE_FREE0, FB_STAGE_FREE1, FB_S_FULL, FB_A_FULL,
-    FB_O_FULL, FB_O_FREE, FB_AV_DONE, FB_PHIQ_FULL, FB_PHIQ_FREE, FB_PHIK_FULL, FB_PHIK_FREE,
-    FB_UPD_DONE, FB_SBF_FULL, FB_DRAIN, FB_COUNT
+    FB_TMA_FULL0 = 0, FB_STAGE_FREE0 = 3, FB_S_FULL = 6, FB_A_FULL, FB_O_FULL0, FB_O_FULL1,
+    FB_O_FREE0, FB_O_FREE1, FB_AV_DONE, FB_PHIQ_FULL, FB_PHIQ_FREE, FB_PHIK_FULL, FB_PHIK_FREE,
+    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_COUNT
 };
 
 template <int K, int V>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, float *__restrict__ out,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G,
                  float scale) {
     using CF = Cfg<K, V>;
+    constexpr bool FAST = CF::FAST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -283,32 +365,34 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const long long g0 = part.g0, g1 = part.g1;
     const int nchunks = static_cast<int>(g1 - g0);
     if (nchunks <= 0) return;
+    BASED_TRACE_INIT;
 
     // ---- set-up: barriers, constant tiles, TMEM -------------------------------------------------
     if (threadIdx.x == 0) {
-        const uint32_t counts[FB_COUNT] = {1, 1, 1, 1, 1, 4, 1, 4, 1, 4, 1, 4, 1, 1, 4, 1};
+        // arrivals per phase: 1 = producer / commit, 4 = one elected lane per warp of a group
+        const uint32_t counts[FB_COUNT] = {1, 1, 1, 1, 1, 1, 1, 4, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, 4, 4, 1};
         for (int i = 0; i < FB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // bf16 state operand: zero once (rows V+2.. stay zero; rows 0..V+1 are rewritten per use).
-    for (int i = threadIdx.x; i < CF::SBF / 16; i += kFwdThreads)
+    // bf16 state operands: zero once (rows V+2.. stay zero; rows 0..V+1 are rewritten per use).
+    for (int i = threadIdx.x; i < CF::NSBF * CF::SBF / 16; i += kFwdThreads)
         st_shared_v4(sb + CF::OFF_SBF + 16u * i, 0u, 0u, 0u, 0u);
     if constexpr (CF::ZROW) {
-        // ones tile: the extra A rows (64..127) of the state update, as an MN-major SW128 block;
-        // row (token) r holds 1.0 at element 0, so that row 64 of S^T accumulates z.
-        for (int i = threadIdx.x; i < CF::VT / 16; i += kFwdThreads)
+        // ones block: an MN-major SW128 block whose element 0 is 1.0 in every token row. It is
+        // the extra operand block behind v_c: A rows 64..127 of the state update (so that row 64
+        // of S^T accumulates z) and B columns 64..79 of A [v | 1] (column 64 = rowsum A).
+        for (int i = threadIdx.x; i < CF::ONES / 16; i += kFwdThreads)
             st_shared_v4(sb + CF::OFF_ONES + 16u * i, 0u, 0u, 0u, 0u);
         __syncthreads();
-        if (threadIdx.x < kChunk)
+        if (threadIdx.x < 16)
             st_shared_u16(sb + CF::OFF_ONES + sw128(threadIdx.x, 0), 0x3F80);
-    } else {
-        // ones column for the z MMA: K-major SW32 operand, N row 0 = 16 ones, rows 1..15 = 0.
-        if (threadIdx.x < 32)
-            st_shared_v4(sb + CF::OFF_ZONES + 16u * threadIdx.x,
-                         threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u,
-                         threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u);
     }
+    // ones column as a K-major SW32 operand: N row 0 = 16 ones, rows 1..15 = 0.
+    if (threadIdx.x < 32)
+        st_shared_v4(sb + CF::OFF_ZONES + 16u * threadIdx.x, threadIdx.x < 2 ? 0x3F803F80u : 0u,
+                     threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u,
+                     threadIdx.x < 2 ? 0x3F803F80u : 0u);
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_holder), 512);
         tmem_relinquish();
@@ -319,127 +403,158 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    const float c_lin = scale, c_sq = 0.5f * scale * scale, c_x = scale * scale;
-
     if (warp == 0) {
         // ================================ TMA producer =========================================
         if (lane == 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_o);
             int issued = 0;
-            for (int n = 0; n < nchunks; ++n) {
-                const int s = n & 1;
-                if (n >= 2 && !wait_bar(BAR(FB_STAGE_FREE0 + s), ((n >> 1) - 1) & 1, abort_flag,
-                                        SITE_STAGE_FREE))
+            Cursor cu;
+            cu.init(g0, nchunks, n_c, H);
+            for (int n = 0; n < nchunks; ++n, cu.next()) {
+                const int s = n % CF::NST;
+                if (n >= CF::NST && !wait_bar(BAR(FB_STAGE_FREE0 + s), ((n / CF::NST) - 1) & 1,
+                                              abort_flag, SITE_STAGE_FREE))
                     break;
-                const ChunkInfo ci = chunk_info(g0 + n, g1, n_c, H);
                 const uint32_t bar = BAR(FB_TMA_FULL0 + s);
+                BASED_TRACE_EV(n, TE_TMA_ISSUE);
                 mbar_arrive_expect_tx(bar, 2 * CF::RAW + CF::VT);
-                tma_load_4d(sb + CF::OFF_RAWQ + s * CF::RAW, &tm_q, bar, 0, ci.h, ci.t0, ci.b);
-                tma_load_4d(sb + CF::OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, ci.h, ci.t0, ci.b);
-                tma_load_4d(sb + CF::OFF_V + s * CF::VT, &tm_v, bar, 0, ci.h, ci.t0, ci.b);
+                tma_load_4d(sb + CF::OFF_RAWQ + s * CF::RAW, &tm_q, bar, 0, cu.h, cu.t0(), cu.b);
+                tma_load_4d(sb + CF::OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
+                tma_load_4d(sb + CF::OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
                 if constexpr (V == 128)
-                    tma_load_4d(sb + CF::OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, ci.h, ci.t0,
-                                ci.b);
+                    tma_load_4d(sb + CF::OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(),
+                                cu.b);
                 ++issued;
             }
             if (*abort_flag) {  // let copies already in flight land before the CTA exits
-                for (int m = issued - 2; m < issued; ++m)
+                for (int m = issued - CF::NST; m < issued; ++m)
                     if (m >= 0)
-                        wait_bar(BAR(FB_TMA_FULL0 + (m & 1)), (m >> 1) & 1, nullptr, SITE_DRAIN,
-                                 kDrainLimitNs);
+                        wait_bar(BAR(FB_TMA_FULL0 + m % CF::NST), (m / CF::NST) & 1, nullptr,
+                                 SITE_DRAIN, kDrainLimitNs);
             }
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ===========================================
         if (lane == 0) {
-            const uint32_t t_s = tmem + CF::TM_S, t_sa = tmem + CF::TM_SA, t_o = tmem + CF::TM_O,
+            const uint32_t t_s = tmem + CF::TM_S, t_sc = tmem + CF::TM_SC, t_a = tmem + CF::TM_A,
                            t_z = tmem + CF::TM_Z;
+            const uint32_t t_o0 = tmem + CF::TM_O0, t_o1 = tmem + CF::TM_O1;
             constexpr uint32_t ID_QK = idesc_bf16_f32(128, 128, 0, 0);
-            constexpr uint32_t ID_AV = idesc_bf16_f32(128, V, 0, 1);
+            constexpr uint32_t ID_AV = idesc_bf16_f32(128, FAST ? CF::NO : V, 0, 1);
+            constexpr uint32_t ID_RS = idesc_bf16_f32(128, 16, 0, 0);
             constexpr uint32_t ID_RO = idesc_bf16_f32(128, CF::NO, 0, 0);
             constexpr uint32_t ID_UPD = idesc_bf16_f32(128, CF::PP, 1, 1);
             constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
-            auto issue_qk = [&](int s) {
-                const uint64_t a = smem_desc(sb + CF::OFF_RAWQ + s * CF::RAW, 16, 256, LAYOUT_SW32);
-                const uint64_t b = smem_desc(sb + CF::OFF_RAWK + s * CF::RAW, 16, 256, LAYOUT_SW32);
-                mma_ss(t_sa, a, b, ID_QK, 0);
+            // Operand descriptors, computed once: per k-step and per stage only the start address
+            // advances. Raw q/k tiles are K-major SW32; v_c is an MN-major SW128 operand whose
+            // second 64-wide block is the ones block (V = 64, LBO depends on the stage) or the
+            // upper half of v_c (V = 128).
+            const uint64_t d_q = smem_desc(sb + CF::OFF_RAWQ, 16, 256, LAYOUT_SW32);
+            const uint64_t d_k = smem_desc(sb + CF::OFF_RAWK, 16, 256, LAYOUT_SW32);
+            auto va_desc = [&](int s) {  // k-step 0 of stage s
+                const uint32_t lbo = CF::ZROW ? CF::OFF_ONES - CF::OFF_V - s * CF::VT : 16384u;
+                return smem_desc(sb + CF::OFF_V + s * CF::VT, lbo, 1024, LAYOUT_SW128);
             };
+            const uint64_t d_va0 = va_desc(0), d_va1 = va_desc(1), d_va2 = va_desc(CF::NST > 2 ? 2 : 1);
+            const uint64_t d_sbf0 = smem_desc(sb + CF::OFF_SBF, 16, 256, LAYOUT_SW32);
+            const uint64_t d_sbf1 = smem_desc(sb + CF::OFF_SBF + (CF::NSBF - 1) * CF::SBF, 16, 256, LAYOUT_SW32);
+            const uint64_t d_phik = smem_desc(sb + CF::OFF_PHIK, 4096, 256, LAYOUT_SW32);
+            const uint64_t d_phiq = smem_desc(sb + CF::OFF_PHIQ, 16, 256, LAYOUT_SW32);
+            const uint64_t d_zones = smem_desc(sb + CF::OFF_ZONES, 16, 256, LAYOUT_SW32);
+
             int ro_idx = 0, upd_idx = 0;
             bool ok = wait_bar(BAR(FB_TMA_FULL0), 0, abort_flag, SITE_TMA_FULL);
             if (ok) {
                 tc_fence_after();
-                issue_qk(0);
+                mma_ss(t_sc, d_q, d_k, ID_QK, 0);
                 mma_commit(BAR(FB_S_FULL));
             }
-            for (int n = 0; ok && n < nchunks; ++n) {
-                const int s = n & 1;
-                const ChunkInfo ci = chunk_info(g0 + n, g1, n_c, H);
-                if (!(ok = wait_bar(BAR(FB_A_FULL), n & 1, abort_flag, SITE_A_FULL))) break;
-                if (n > 0 && !(ok = wait_bar(BAR(FB_O_FREE), (n - 1) & 1, abort_flag, SITE_O_FREE)))
-                    break;
+            auto issue_ro = [&](uint32_t t_out) -> bool {
+                // O += f~(q_c) [S | z_hi z_lo]
+                if (!wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)) return false;
+                if (!wait_bar(BAR(FB_SBF_FULL), ro_idx & 1, abort_flag, SITE_SBF_FULL)) return false;
                 tc_fence_after();
-                // O = A v_c (A: bf16 in TMEM; v_c: MN-major SW128, 16 tokens per step)
-                const uint32_t vb = sb + CF::OFF_V + s * CF::VT;
+                const uint64_t db = (ro_idx & 1) ? d_sbf1 : d_sbf0;
+#pragma unroll
+                for (int f = 0; f < CF::NBLK; ++f)
+                    mma_ss(t_out, dadd(d_phiq, 4096 * f), dadd(db, CF::SBF_BLK * f), ID_RO, 1);
+                mma_commit(BAR(FB_PHIQ_FREE));
+                ++ro_idx;
+                return true;
+            };
+            Cursor cu;
+            cu.init(g0, nchunks, n_c, H);
+            for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
+                const int s = n % CF::NST;
+                const int ob = FAST ? (n & 1) : 0;
+                const uint64_t d_va = s == 0 ? d_va0 : (s == 1 ? d_va1 : d_va2);
+                const uint32_t t_out = ob ? t_o1 : t_o0;
+                if (!(ok = wait_bar(BAR(FB_A_FULL), n & 1, abort_flag, SITE_A_FULL))) break;
+                BASED_TRACE_EV(n, TE_A_READY);
+                if (FAST ? (n >= 2) : (n >= 1)) {
+                    const uint32_t par = FAST ? (((n >> 1) - 1) & 1) : ((n - 1) & 1);
+                    if (!(ok = wait_bar(BAR(FB_O_FREE0 + ob), par, abort_flag, SITE_O_FREE))) break;
+                }
+                tc_fence_after();
+                // O = A [v_c | 1]: numerators and rowsum A (V = 64: one MMA per 16 keys over the
+                // v block and the ones block; V = 128: a separate 16-column MMA for the rowsum)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    mma_ts(t_o, t_sa + 8 * j, smem_desc(vb + 2048 * j, 16384, 1024, LAYOUT_SW128),
-                           ID_AV, j > 0);
-                mma_commit(BAR(FB_AV_DONE));
-                if (ci.has_ro) {
-                    // O += f(q_c) [S | z_hi z_lo]
-                    if (!(ok = wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)))
-                        break;
-                    if (!(ok = wait_bar(BAR(FB_SBF_FULL), ro_idx & 1, abort_flag, SITE_SBF_FULL)))
-                        break;
-                    tc_fence_after();
+                    mma_ts(t_out, t_a + 8 * j, v_step<CF::ZROW>(d_va, j), ID_AV, j > 0);
+                BASED_TRACE_EV(n, TE_AV_ISSUED);
+                if constexpr (!FAST) {
 #pragma unroll
-                    for (int f = 0; f < CF::NBLK; ++f)
-                        mma_ss(t_o, smem_desc(sb + CF::OFF_PHIQ + 4096 * f, 16, 256, LAYOUT_SW32),
-                               smem_desc(sb + CF::OFF_SBF + CF::SBF_BLK * f, 16, 256, LAYOUT_SW32),
-                               ID_RO, 1);
-                    mma_commit(BAR(FB_PHIQ_FREE));
-                    ++ro_idx;
+                    for (int j = 0; j < 8; ++j) mma_ts(t_out + V, t_a + 8 * j, d_zones, ID_RS, j > 0);
+                    mma_commit(BAR(FB_AV_DONE));
+                    if (cu.has_ro() && !(ok = issue_ro(t_out))) break;
+                    mma_commit(BAR(FB_O_FULL0));
+                    BASED_TRACE_EV(n, TE_RO_ISSUED);
+                    // the next s overwrites A (same TMEM columns): wait until A has been read
+                    if (!(ok = wait_bar(BAR(FB_AV_DONE), n & 1, abort_flag, SITE_AV_DONE))) break;
                 }
-                mma_commit(BAR(FB_O_FULL));
-                // s of the next chunk overwrites A: wait until the A v_c product has read it.
-                if (!(ok = wait_bar(BAR(FB_AV_DONE), n & 1, abort_flag, SITE_AV_DONE))) break;
                 if (n + 1 < nchunks) {
-                    const int s1 = (n + 1) & 1;
-                    if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s1), ((n + 1) >> 1) & 1, abort_flag,
+                    const int s1 = (n + 1) % CF::NST;
+                    if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s1), ((n + 1) / CF::NST) & 1, abort_flag,
                                         SITE_TMA_FULL)))
                         break;
                     tc_fence_after();
-                    issue_qk(s1);
+                    mma_ss(t_sc, dadd(d_q, s1 * CF::RAW), dadd(d_k, s1 * CF::RAW), ID_QK, 0);
                     mma_commit(BAR(FB_S_FULL));
+                    BASED_TRACE_EV(n, TE_QK_ISSUED);
                 }
-                if (ci.has_upd) {
-                    // S^T += [v_c | 1]^T f(k_c)  (and z via the ones row or the z MMA)
+                if (cu.has_upd()) {
+                    // S^T += [v_c | 1]^T f(k_c)  (z as row 64, or via the z MMAs)
                     if (!(ok = wait_bar(BAR(FB_PHIK_FULL), upd_idx & 1, abort_flag, SITE_PHIK_FULL)))
                         break;
+                    if (cu.upd_acc()) {
+                        // the previous conversion must have read S^T before it changes
+                        const int r = FAST ? ro_idx : ro_idx - 1;
+                        if (!(ok = wait_bar(BAR(FB_CONV_READ), r & 1, abort_flag, SITE_CONV_READ)))
+                            break;
+                    }
                     tc_fence_after();
-                    const uint32_t lbo_a = CF::ZROW ? (CF::OFF_ONES - (CF::OFF_V + s * CF::VT)) : 16384u;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const uint32_t acc = (j > 0 || ci.upd_acc) ? 1u : 0u;
-                        mma_ss(t_s, smem_desc(vb + 2048 * j, lbo_a, 1024, LAYOUT_SW128),
-                               smem_desc(sb + CF::OFF_PHIK + 512 * j, 4096, 256, LAYOUT_SW32),
-                               ID_UPD, acc);
+                        const uint32_t acc = (j > 0 || cu.upd_acc()) ? 1u : 0u;
+                        mma_ss(t_s, v_step<CF::ZROW>(d_va, j), dadd(d_phik, 512 * j), ID_UPD, acc);
                         if constexpr (!CF::ZROW) {
-                            const uint64_t zb = smem_desc(sb + CF::OFF_ZONES, 16, 256, LAYOUT_SW32);
-                            mma_ss(t_z, smem_desc(sb + CF::OFF_PHIK + 512 * j, 4096, 256, LAYOUT_SW32),
-                                   zb, ID_Z, acc);
+                            mma_ss(t_z, dadd(d_phik, 512 * j), d_zones, ID_Z, acc);
                             if constexpr (CF::PP > 128)  // features 32..159 (only 128.. read)
-                                mma_ss(t_z + 16,
-                                       smem_desc(sb + CF::OFF_PHIK + 2 * 4096 + 512 * j, 4096, 256,
-                                                 LAYOUT_SW32),
-                                       zb, ID_Z, acc);
+                                mma_ss(t_z + 16, dadd(d_phik, 2 * 4096 + 512 * j), d_zones, ID_Z, acc);
                         }
                     }
                     mma_commit(BAR(FB_UPD_DONE));
                     mma_commit(BAR(FB_PHIK_FREE));
+                    BASED_TRACE_EV(n, TE_UPD_ISSUED);
                     ++upd_idx;
+                }
+                if constexpr (FAST) {
+                    if (cu.has_ro() && !(ok = issue_ro(t_out))) break;
+                    mma_commit(BAR(FB_O_FULL0 + ob));
+                    BASED_TRACE_EV(n, TE_RO_ISSUED);
                 }
                 mma_commit(BAR(FB_STAGE_FREE0 + s));
             }
@@ -450,125 +565,181 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (warp < 4) {
         // warps 2 and 3: no role (warp 2 owns the TMEM allocation)
     } else if (warp < 8) {
-        // ======================= rows: polynomial of chunk n, epilogue of chunk n-1 ============
+        // ======================= Taylor weights: A = poly(s), causal mask =======================
         const int q4 = warp & 3;
-        const int row = q4 * 32 + lane;
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
         const float c1 = scale, c2 = 0.5f * scale * scale;
-        tmem_st_x2(tmem + lo + CF::TM_O + V, 0u, 0u);  // den columns start at zero
-        tmem_wait_st();
-
-        auto epilogue = [&](int m, float rowsum) -> bool {
-            const ChunkInfo ci = chunk_info(g0 + m, g1, n_c, H);
-            if (!wait_bar(BAR(FB_O_FULL), m & 1, abort_flag, SITE_O_FULL)) return false;
-            tc_fence_after();
-            uint32_t d[2];
-            tmem_ld_x2(tmem + lo + CF::TM_O + V, d);
-            uint32_t r[32];
-            tmem_ld_x32(tmem + lo + CF::TM_O, r);
-            tmem_wait_ld();
-            const float den = rowsum + __uint_as_float(d[0]) + __uint_as_float(d[1]) + 1e-6f;
-            const float inv = __frcp_rn(den);
-            const int t = ci.t0 + row;
-            float *dst = out + ((static_cast<size_t>(ci.b) * T + t) * H + ci.h) * V;
-            const bool valid = t < T;
+        const uint64_t C1 = pack_f32x2(c1, c1), C2 = pack_f32x2(c2, c2), ONE = pack_f32x2(1.f, 1.f);
+        if constexpr (FAST) {
+            // A blocks above the diagonal block stay zero (never rewritten)
+            uint32_t z16[16];
 #pragma unroll
-            for (int p = 0; p < V / 32; ++p) {
-                if (p > 0) {
-                    tmem_ld_x32(tmem + lo + CF::TM_O + 32 * p, r);
-                    tmem_wait_ld();
-                }
-                if (p == V / 32 - 1) {
-                    // O fully read: zero the den columns for the next chunk and release O.
-                    tmem_st_x2(tmem + lo + CF::TM_O + V, 0u, 0u);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(FB_O_FREE));
-                }
-                if (valid) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        st_global_cs_v4(dst + 32 * p + e, __uint_as_float(r[e]) * inv,
-                                        __uint_as_float(r[e + 1]) * inv,
-                                        __uint_as_float(r[e + 2]) * inv,
-                                        __uint_as_float(r[e + 3]) * inv);
-                }
-            }
-            return true;
+            for (int j = 0; j < 16; ++j) z16[j] = 0u;
+            for (int kb = q4 + 1; kb < 4; ++kb) tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, z16);
+            tmem_wait_st();
+        }
+        // mask of the diagonal block, per bf16 pair (keys 2i, 2i+1 against row = lane)
+        auto diag_mask = [&](int i) -> uint32_t {
+            return (2 * i <= lane ? 0x0000FFFFu : 0u) | (2 * i + 1 <= lane ? 0xFFFF0000u : 0u);
         };
-
-        float rs_prev = 0.0f;
-        bool ok = true;
         for (int n = 0; n < nchunks; ++n) {
-            if (!(ok = wait_bar(BAR(FB_S_FULL), n & 1, abort_flag, SITE_S_FULL))) break;
+            if (!wait_bar(BAR(FB_S_FULL), n & 1, abort_flag, SITE_S_FULL)) break;
             tc_fence_after();
-            float rs = 0.0f;
+            if (warp == 7 && lane == 0) BASED_TRACE_EV(n, TE_POLY_BEGIN);
+            uint32_t z16[16];
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) {
-                uint32_t packed[16];
-                if (kb <= q4) {
-                    uint32_t r[32];
-                    tmem_ld_x32(tmem + lo + CF::TM_SA + 32 * kb, r);
+            for (int j = 0; j < 16; ++j) z16[j] = 0u;
+#pragma unroll
+            for (int kp = 0; kp < 4; kp += 2) {
+                // two key blocks per TMEM round trip; blocks above the diagonal block are zero
+                if (kp <= q4) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * kp, r0);
+                    if (kp + 1 <= q4) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kp + 1), r1);
                     tmem_wait_ld();
+                    if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kp == 0 ? TE_POLY_LD0 : TE_POLY_LD1);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float s0 = __uint_as_float(r[j]), s1 = __uint_as_float(r[j + 1]);
-                        float a0 = fmaf(s0, fmaf(c2, s0, c1), 1.0f);
-                        float a1 = fmaf(s1, fmaf(c2, s1, c1), 1.0f);
-                        if (kb == q4) {  // causal mask on the diagonal block: key j <= row
-                            if (j > lane) a0 = 0.0f;
-                            if (j + 1 > lane) a1 = 0.0f;
+                    for (int h = 0; h < 2; ++h) {
+                        const int kb = kp + h;
+                        if (kb > q4) break;
+                        const uint32_t *r = h ? r1 : r0;
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            packed[i] = taylor2(r[2 * i], r[2 * i + 1], C2, C1, ONE);
+                            if (kb == q4) packed[i] &= diag_mask(i);
                         }
-                        const __nv_bfloat162 p = __floats2bfloat162_rn(a0, a1);
-                        rs += __low2float(p) + __high2float(p);
-                        packed[j >> 1] = *reinterpret_cast<const uint32_t *>(&p);
+                        // V = 128: A columns [16 kb, 16 kb + 16) overlay s columns already read
+                        tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, packed);
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) packed[j] = 0u;
+                    if (!FAST && kp + 1 > q4) tmem_st_x16(tmem + lo + CF::TM_A + 16 * (kp + 1), z16);
+                    if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kp == 0 ? TE_POLY_ST0 : TE_POLY_ST1);
+                } else if (!FAST) {
+                    tmem_st_x16(tmem + lo + CF::TM_A + 16 * kp, z16);
+                    tmem_st_x16(tmem + lo + CF::TM_A + 16 * (kp + 1), z16);
                 }
-                // A columns [16 kb, 16 kb + 16) overlay s columns that were already read.
-                tmem_st_x16(tmem + lo + CF::TM_SA + 16 * kb, packed);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_A_FULL));
-            if (n > 0 && !(ok = epilogue(n - 1, rs_prev))) break;
-            rs_prev = rs;
+            if (warp == 7 && lane == 0) BASED_TRACE_EV(n, TE_POLY_END);
         }
-        if (ok) epilogue(nchunks - 1, rs_prev);
     } else if (warp < 12) {
-        // ================================ feature builders =====================================
-        const int t = (warp - 8) * 32 + lane;
+        // =============== feature tiles f(k_c), f~(q_c) and the output epilogue ==================
+        const int t = (warp - 8) * 32 + lane;  // token of the chunk = TMEM lane = output row
+        const int q4 = warp & 3;
+        const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
+        const uint32_t sig2 = pack_bf16x2(scale, scale);
         int ro_idx = 0, upd_idx = 0;
-        for (int n = 0; n < nchunks; ++n) {
-            const int s = n & 1;
-            const ChunkInfo ci = chunk_info(g0 + n, g1, n_c, H);
-            if (!ci.has_ro && !ci.has_upd) continue;
-            if (!wait_bar(BAR(FB_TMA_FULL0 + s), (n >> 1) & 1, abort_flag, SITE_TMA_FULL)) break;
-            if (ci.has_ro) {
-                if (ro_idx > 0 &&
-                    !wait_bar(BAR(FB_PHIQ_FREE), (ro_idx - 1) & 1, abort_flag, SITE_PHIQ_FREE))
-                    break;
-                build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t);
-                fence_proxy_async_smem();
+        bool ok = true;
+
+        // Output tile: o = O_num / (O_den + 1e-6), written through a 16 KB staging buffer as
+        // 32-column pieces (128 rows x 128 B, SW128) by TMA stores, so that the output traffic
+        // never occupies the load/store path the TMEM accesses of the other roles use. Rows past T
+        // are clipped by the tensor map.
+        const uint32_t ost = sb + CF::OFF_OST;
+        auto epilogue = [&](int m, int eb, int eh, int et0) -> bool {
+            const int ob = FAST ? (m & 1) : 0;
+            const uint32_t par = FAST ? ((m >> 1) & 1) : (m & 1);
+            if (!wait_bar(BAR(FB_O_FULL0 + ob), par, abort_flag, SITE_O_FULL)) return false;
+            tc_fence_after();
+            if (warp == 11 && lane == 0) BASED_TRACE_EV(m, TE_EPI_BEGIN);
+            const uint32_t to = tmem + lo + (ob ? CF::TM_O1 : CF::TM_O0);
+            uint32_t d[2], r0[32], r1[32];
+            tmem_ld_x2(to + V, d);
+            tmem_ld_x32(to, r0);
+            tmem_ld_x32(to + 32, r1);
+            tmem_wait_ld();
+            const float inv = __frcp_rn(__uint_as_float(d[0]) + __uint_as_float(d[1]) + 1e-6f);
+            auto release_o = [&]() {
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(FB_PHIQ_FULL));
-                ++ro_idx;
-            }
-            if (ci.has_upd) {
-                if (upd_idx > 0 &&
-                    !wait_bar(BAR(FB_PHIK_FREE), (upd_idx - 1) & 1, abort_flag, SITE_PHIK_FREE))
-                    break;
-                build_features<K>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t);
+                if (lane == 0) mbar_arrive(BAR(FB_O_FREE0 + ob));  // O read completely
+                if (warp == 11 && lane == 0) BASED_TRACE_EV(m, TE_EPI_OFREE);
+            };
+            if constexpr (V == 64) release_o();
+#pragma unroll
+            for (int p = 0; p < V / 32; ++p) {
+                if constexpr (V == 128) {
+                    if (p == 2) {
+                        tmem_ld_x32(to + 64, r0);
+                        tmem_ld_x32(to + 96, r1);
+                        tmem_wait_ld();
+                        release_o();
+                    }
+                }
+                const uint32_t *r = (p & 1) ? r1 : r0;
+                if (t == 0) bulk_wait_group_read<0>();  // previous piece has left the buffer
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(ost + static_cast<uint32_t>(t) * 128u + ((c ^ (t & 7)) << 4),
+                                 __float_as_uint(__uint_as_float(r[4 * c]) * inv),
+                                 __float_as_uint(__uint_as_float(r[4 * c + 1]) * inv),
+                                 __float_as_uint(__uint_as_float(r[4 * c + 2]) * inv),
+                                 __float_as_uint(__uint_as_float(r[4 * c + 3]) * inv));
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(FB_PHIK_FULL));
-                ++upd_idx;
+                named_bar_sync(1, 128);
+                if (t == 0) {
+                    tma_store_4d(&tm_o, ost, 32 * p, eh, et0, eb);
+                    bulk_commit_group();
+                }
             }
+            if (warp == 11 && lane == 0) BASED_TRACE_EV(m, TE_EPI_END);
+            return true;
+        };
+        auto build_q = [&](int n, int s) -> bool {
+            if (ro_idx > 0 &&
+                !wait_bar(BAR(FB_PHIQ_FREE), (ro_idx - 1) & 1, abort_flag, SITE_PHIQ_FREE))
+                return false;
+            if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_BEGIN);
+            build_features<K, true>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, sig2);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(FB_PHIQ_FULL));
+            if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_END);
+            ++ro_idx;
+            return true;
+        };
+        auto build_k = [&](int n, int s) -> bool {
+            if (upd_idx > 0 &&
+                !wait_bar(BAR(FB_PHIK_FREE), (upd_idx - 1) & 1, abort_flag, SITE_PHIK_FREE))
+                return false;
+            if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIK_BEGIN);
+            build_features<K, false>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(FB_PHIK_FULL));
+            if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIK_END);
+            ++upd_idx;
+            return true;
+        };
+        Cursor cu;
+        cu.init(g0, nchunks, n_c, H);
+        int pb = 0, ph = 0, pt0 = 0;  // coordinates of the previous chunk (for its epilogue)
+        for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
+            const int s = n % CF::NST;
+            if (!FAST && n > 0 && !(ok = epilogue(n - 1, pb, ph, pt0))) break;
+            if (cu.has_ro() || cu.has_upd()) {
+                if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s), (n / CF::NST) & 1, abort_flag,
+                                    SITE_TMA_FULL)))
+                    break;
+                if (FAST) {  // the state update comes first in the MMA order
+                    if (cu.has_upd() && !(ok = build_k(n, s))) break;
+                    if (cu.has_ro() && !(ok = build_q(n, s))) break;
+                } else {
+                    if (cu.has_ro() && !(ok = build_q(n, s))) break;
+                    if (cu.has_upd() && !(ok = build_k(n, s))) break;
+                }
+            }
+            if (FAST && n > 0 && !(ok = epilogue(n - 1, pb, ph, pt0))) break;
+            pb = cu.b;
+            ph = cu.h;
+            pt0 = cu.t0();
         }
+        if (ok) epilogue(nchunks - 1, pb, ph, pt0);
+        if (t == 0) bulk_wait_group_all();  // the staging buffer must outlive the last store
     } else {
         // ============== state conversion: S^T (fp32, TMEM) -> bf16 operand [S | z_hi z_lo] =====
         const int q4 = warp & 3;
@@ -576,65 +747,96 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
         constexpr int LAST_ROW = CF::ZROW ? V : V - 1;
         const bool warp_has_rows = q4 * 32 <= LAST_ROW;
+        constexpr int BATCH = V == 64 ? (CF::NBLK + 1) / 2 : 4;  // blocks per TMEM round trip
 
-        auto convert = [&]() {
-            if (warp_has_rows) {
-#pragma unroll 1
-                for (int f = 0; f < CF::NBLK; ++f) {
-                    uint32_t x[16];
-                    tmem_ld_x16(tmem + lo + CF::TM_S + 16 * f, x);
-                    tmem_wait_ld();
-                    float v[16];
+        auto put_block = [&](uint32_t sbf, int f, const uint32_t *x) {
+            const uint32_t blk = sbf + CF::SBF_BLK * f;
+            if (r < V) {
+                st_shared_v4(blk + sw32(r, 0), pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                             pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                             pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                             pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                st_shared_v4(blk + sw32(r, 1), pack_bf16x2(__uint_as_float(x[8]), __uint_as_float(x[9])),
+                             pack_bf16x2(__uint_as_float(x[10]), __uint_as_float(x[11])),
+                             pack_bf16x2(__uint_as_float(x[12]), __uint_as_float(x[13])),
+                             pack_bf16x2(__uint_as_float(x[14]), __uint_as_float(x[15])));
+            } else if (CF::ZROW && r == V) {
+                // z as a hi/lo pair of bf16 rows: about 16 significant bits
+                uint32_t hi[8], lw[8];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        v[j] = __uint_as_float(x[j]) * feature_coef<K>(f, j, c_lin, c_sq, c_x);
-                    const uint32_t blk = sb + CF::OFF_SBF + CF::SBF_BLK * f;
-                    if (r < V) {
-                        st_shared_v4(blk + sw32(r, 0), pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                     pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-                        st_shared_v4(blk + sw32(r, 1), pack_bf16x2(v[8], v[9]),
-                                     pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
-                                     pack_bf16x2(v[14], v[15]));
-                    } else if (CF::ZROW && r == V) {
-                        // z as a hi/lo pair of bf16 rows: about 16 significant bits
-                        uint32_t hi[8], lw[8];
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j], v[j + 1]);
-                            hi[j >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
-                            lw[j >> 1] = pack_bf16x2(v[j] - __low2float(h2), v[j + 1] - __high2float(h2));
-                        }
-                        st_shared_v4(blk + sw32(V, 0), hi[0], hi[1], hi[2], hi[3]);
-                        st_shared_v4(blk + sw32(V, 1), hi[4], hi[5], hi[6], hi[7]);
-                        st_shared_v4(blk + sw32(V + 1, 0), lw[0], lw[1], lw[2], lw[3]);
-                        st_shared_v4(blk + sw32(V + 1, 1), lw[4], lw[5], lw[6], lw[7]);
-                    }
+                for (int j = 0; j < 16; j += 2) {
+                    const float a = __uint_as_float(x[j]), b = __uint_as_float(x[j + 1]);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+                    hi[j >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
+                    lw[j >> 1] = pack_bf16x2(a - __low2float(h2), b - __high2float(h2));
                 }
+                st_shared_v4(blk + sw32(V, 0), hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(blk + sw32(V, 1), hi[4], hi[5], hi[6], hi[7]);
+                st_shared_v4(blk + sw32(V + 1, 0), lw[0], lw[1], lw[2], lw[3]);
+                st_shared_v4(blk + sw32(V + 1, 1), lw[4], lw[5], lw[6], lw[7]);
+            }
+        };
+        auto put_z = [&](uint32_t sbf, int p, float z) {
+            const int f = p >> 4, j = p & 15;
+            const __nv_bfloat16 h = __float2bfloat16_rn(z);
+            const __nv_bfloat16 l = __float2bfloat16_rn(z - __bfloat162float(h));
+            const uint32_t a = sbf + CF::SBF_BLK * f + 2u * (j & 7);
+            st_shared_u16(a + sw32(V, j >> 3), *reinterpret_cast<const uint16_t *>(&h));
+            st_shared_u16(a + sw32(V + 1, j >> 3), *reinterpret_cast<const uint16_t *>(&l));
+        };
+        auto convert = [&](int cidx, int n) -> bool {
+            // SBF_FULL counts one arrival per conversion warp; a warp must not arrive for this
+            // conversion while the previous phase is still open (a warp without rows finishes
+            // early, and the next state update only waits for CONV_READ).
+            if (cidx > 0 && !wait_bar(BAR(FB_SBF_FULL), (cidx - 1) & 1, abort_flag, SITE_SBF_FULL))
+                return false;
+            if (warp == 12 && lane == 0) BASED_TRACE_EV(n, TE_CONV_BEGIN);
+            const uint32_t sbf = sb + CF::OFF_SBF + (cidx % CF::NSBF) * CF::SBF;
+            float za = 0.f, zb = 0.f;
+            if constexpr (!CF::ZROW) {
+                uint32_t a, b;
+                tmem_ld_x1(tmem + lo + CF::TM_Z, a);
+                tmem_ld_x1(tmem + lo + CF::TM_Z + 16, b);
+                tmem_wait_ld();
+                za = __uint_as_float(a);
+                zb = __uint_as_float(b);
+            }
+            if (warp_has_rows) {
+                // BATCH feature blocks per TMEM round trip; S^T is released after the last load
+#pragma unroll
+                for (int f0 = 0; f0 < CF::NBLK; f0 += BATCH) {
+                    uint32_t x[BATCH][16];
+#pragma unroll
+                    for (int f = 0; f < BATCH; ++f)
+                        if (f0 + f < CF::NBLK) tmem_ld_x16(tmem + lo + CF::TM_S + 16 * (f0 + f), x[f]);
+                    tmem_wait_ld();
+                    if (f0 + BATCH >= CF::NBLK) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(BAR(FB_CONV_READ));  // S^T may change now
+                        if (warp == 12 && lane == 0) BASED_TRACE_EV(n, TE_CONV_READ);
+                    }
+#pragma unroll
+                    for (int f = 0; f < BATCH; ++f)
+                        if (f0 + f < CF::NBLK) put_block(sbf, f0 + f, x[f]);
+                }
+            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(FB_CONV_READ));
             }
             if constexpr (!CF::ZROW) {
-                // z tiles: lane r of tile a holds feature r, lane r of tile b holds feature r + 32
-                uint32_t za, zb;
-                tmem_ld_x1(tmem + lo + CF::TM_Z, za);
-                tmem_ld_x1(tmem + lo + CF::TM_Z + 16, zb);
-                tmem_wait_ld();
-                auto put = [&](int p, float z) {
-                    const int f = p >> 4, j = p & 15;
-                    const float zc = z * feature_coef<K>(f, j, c_lin, c_sq, c_x);
-                    const __nv_bfloat16 h = __float2bfloat16_rn(zc);
-                    const __nv_bfloat16 l = __float2bfloat16_rn(zc - __bfloat162float(h));
-                    const uint32_t a = sb + CF::OFF_SBF + CF::SBF_BLK * f + 2u * (j & 7);
-                    st_shared_u16(a + sw32(V, j >> 3), *reinterpret_cast<const uint16_t *>(&h));
-                    st_shared_u16(a + sw32(V + 1, j >> 3), *reinterpret_cast<const uint16_t *>(&l));
-                };
-                if (r < CF::PP && r < 128) put(r, __uint_as_float(za));
-                if (r + 32 >= 128 && r + 32 < CF::PP) put(r + 32, __uint_as_float(zb));
+                if (r < CF::PP && r < 128) put_z(sbf, r, za);
+                if (r + 32 >= 128 && r + 32 < CF::PP) put_z(sbf, r + 32, zb);
             }
             fence_proxy_async_smem();
-            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_SBF_FULL));
+            if (warp == 12 && lane == 0) BASED_TRACE_EV(n, TE_CONV_END);
+            return true;
         };
 
+        int cidx = 0;
         // A range that starts inside a head continues from the prefix state of the chunks before
         // it: load it into TMEM, then convert it like any other state.
         if (g0 % n_c != 0) {
@@ -666,15 +868,16 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tmem_st_x1(tmem + lo + CF::TM_Z + 16, __float_as_uint(zb));
             }
             tmem_wait_st();
-            convert();
+            convert(cidx++, 63);
         }
         int u = 0;
-        for (int n = 0; n < nchunks; ++n) {
-            const ChunkInfo ci = chunk_info(g0 + n, g1, n_c, H);
-            if (!ci.has_upd) continue;
+        Cursor cu;
+        cu.init(g0, nchunks, n_c, H);
+        for (int n = 0; n < nchunks; ++n, cu.next()) {
+            if (!cu.has_upd()) continue;
             if (!wait_bar(BAR(FB_UPD_DONE), u & 1, abort_flag, SITE_UPD_DONE)) break;
             tc_fence_after();
-            convert();
+            if (!convert(cidx++, n)) break;
             ++u;
         }
     }
@@ -691,10 +894,13 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // ------------------------------------------------------------------------------------------------
 // Aggregate kernel: the partial state [S^T | z] of the last stretch of a range that ends inside a
 // head, written as fp32 rows into slot blockIdx.x.
+// warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle | warps 4-7: f(k) tiles |
+// warps 8-11: writer
 // ------------------------------------------------------------------------------------------------
 enum AggBar {
-    AB_TMA_FULL0 = 0, AB_TMA_FULL1, AB_STAGE_FREE0, AB_STAGE_FREE1, AB_PHIK_FULL, AB_PHIK_FREE,
-    AB_AGG_DONE, AB_DRAIN, AB_COUNT
+    AB_TMA_FULL0 = 0, AB_STAGE_FREE0 = AB_TMA_FULL0 + kAggStages,
+    AB_PHIK_FULL0 = AB_STAGE_FREE0 + kAggStages, AB_PHIK_FREE0 = AB_PHIK_FULL0 + 2,
+    AB_AGG_DONE = AB_PHIK_FREE0 + 2, AB_COUNT
 };
 
 template <int K, int V>
@@ -702,6 +908,7 @@ __global__ void __launch_bounds__(kAggThreads, 1)
 based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  float *__restrict__ slots, int H, int n_c, long long N, int G) {
     using CF = Cfg<K, V>;
+    constexpr int S = kAggStages;
     if (!has_aggregate(N, G, blockIdx.x, n_c)) return;
     const Part part = cta_range(N, G, blockIdx.x);
     const long long ga = part.g0 > ((part.g1 - 1) / n_c) * n_c ? part.g0 : ((part.g1 - 1) / n_c) * n_c;
@@ -718,23 +925,22 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     auto BAR = [&](int i) -> uint32_t { return sb + CF::A_OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[AB_COUNT] = {1, 1, 1, 1, 4, 1, 1, 1};
-        for (int i = 0; i < AB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
+        for (int i = 0; i < AB_COUNT; ++i)
+            mbar_init(BAR(i), (i == AB_PHIK_FULL0 || i == AB_PHIK_FULL0 + 1) ? 4u : 1u);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if constexpr (CF::ZROW) {
-        for (int i = threadIdx.x; i < CF::VT / 16; i += kAggThreads)
+        for (int i = threadIdx.x; i < CF::ONES / 16; i += kAggThreads)
             st_shared_v4(sb + CF::A_OFF_ONES + 16u * i, 0u, 0u, 0u, 0u);
         __syncthreads();
-        if (threadIdx.x < kChunk)
+        if (threadIdx.x < 16)
             st_shared_u16(sb + CF::A_OFF_ONES + sw128(threadIdx.x, 0), 0x3F80);
-    } else {
-        if (threadIdx.x < 32)
-            st_shared_v4(sb + CF::A_OFF_ZONES + 16u * threadIdx.x,
-                         threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u,
-                         threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u);
     }
+    if (threadIdx.x < 32)
+        st_shared_v4(sb + CF::A_OFF_ZONES + 16u * threadIdx.x, threadIdx.x < 2 ? 0x3F803F80u : 0u,
+                     threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u,
+                     threadIdx.x < 2 ? 0x3F803F80u : 0u);
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_holder), 256);
         tmem_relinquish();
@@ -750,25 +956,26 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
             int issued = 0;
-            for (int n = 0; n < nchunks; ++n) {
-                const int s = n & 1;
-                if (n >= 2 && !wait_bar(BAR(AB_STAGE_FREE0 + s), ((n >> 1) - 1) & 1, abort_flag,
+            Cursor cu;
+            cu.init(ga, nchunks, n_c, H);
+            for (int n = 0; n < nchunks; ++n, cu.next()) {
+                const int s = n % S;
+                if (n >= S && !wait_bar(BAR(AB_STAGE_FREE0 + s), ((n / S) - 1) & 1, abort_flag,
                                         SITE_STAGE_FREE))
                     break;
-                const ChunkInfo ci = chunk_info(ga + n, g1, n_c, H);
                 const uint32_t bar = BAR(AB_TMA_FULL0 + s);
                 mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
-                tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, ci.h, ci.t0, ci.b);
-                tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, ci.h, ci.t0, ci.b);
+                tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
+                tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
                 if constexpr (V == 128)
-                    tma_load_4d(sb + CF::A_OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, ci.h, ci.t0,
-                                ci.b);
+                    tma_load_4d(sb + CF::A_OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(),
+                                cu.b);
                 ++issued;
             }
             if (*abort_flag) {
-                for (int m = issued - 2; m < issued; ++m)
+                for (int m = issued - S; m < issued; ++m)
                     if (m >= 0)
-                        wait_bar(BAR(AB_TMA_FULL0 + (m & 1)), (m >> 1) & 1, nullptr, SITE_DRAIN,
+                        wait_bar(BAR(AB_TMA_FULL0 + (m % S)), (m / S) & 1, nullptr, SITE_DRAIN,
                                  kDrainLimitNs);
             }
         }
@@ -777,31 +984,26 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             constexpr uint32_t ID_UPD = idesc_bf16_f32(128, CF::PP, 1, 1);
             constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
             const uint32_t t_s = tmem, t_z = tmem + CF::TA_Z;
+            const uint64_t d_zones = smem_desc(sb + CF::A_OFF_ZONES, 16, 256, LAYOUT_SW32);
             for (int n = 0; n < nchunks; ++n) {
-                const int s = n & 1;
-                if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n >> 1) & 1, abort_flag, SITE_TMA_FULL)) break;
-                if (!wait_bar(BAR(AB_PHIK_FULL), n & 1, abort_flag, SITE_PHIK_FULL)) break;
+                const int s = n % S, pb = n & 1;
+                if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
+                if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (n >> 1) & 1, abort_flag, SITE_PHIK_FULL)) break;
                 tc_fence_after();
-                const uint32_t vb = sb + CF::A_OFF_V + s * CF::VT;
                 const uint32_t lbo_a = CF::ZROW ? (CF::A_OFF_ONES - (CF::A_OFF_V + s * CF::VT)) : 16384u;
+                const uint64_t d_va = smem_desc(sb + CF::A_OFF_V + s * CF::VT, lbo_a, 1024, LAYOUT_SW128);
+                const uint64_t d_phik = smem_desc(sb + CF::A_OFF_PHIK + pb * CF::PHI, 4096, 256, LAYOUT_SW32);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t acc = (j > 0 || n > 0) ? 1u : 0u;
-                    mma_ss(t_s, smem_desc(vb + 2048 * j, lbo_a, 1024, LAYOUT_SW128),
-                           smem_desc(sb + CF::A_OFF_PHIK + 512 * j, 4096, 256, LAYOUT_SW32), ID_UPD,
-                           acc);
+                    mma_ss(t_s, v_step<CF::ZROW>(d_va, j), dadd(d_phik, 512 * j), ID_UPD, acc);
                     if constexpr (!CF::ZROW) {
-                        const uint64_t zb = smem_desc(sb + CF::A_OFF_ZONES, 16, 256, LAYOUT_SW32);
-                        mma_ss(t_z, smem_desc(sb + CF::A_OFF_PHIK + 512 * j, 4096, 256, LAYOUT_SW32),
-                               zb, ID_Z, acc);
+                        mma_ss(t_z, dadd(d_phik, 512 * j), d_zones, ID_Z, acc);
                         if constexpr (CF::PP > 128)
-                            mma_ss(t_z + 16,
-                                   smem_desc(sb + CF::A_OFF_PHIK + 2 * 4096 + 512 * j, 4096, 256,
-                                             LAYOUT_SW32),
-                                   zb, ID_Z, acc);
+                            mma_ss(t_z + 16, dadd(d_phik, 2 * 4096 + 512 * j), d_zones, ID_Z, acc);
                     }
                 }
-                mma_commit(BAR(AB_PHIK_FREE));
+                mma_commit(BAR(AB_PHIK_FREE0 + pb));
                 mma_commit(BAR(AB_STAGE_FREE0 + s));
             }
             mma_commit(BAR(AB_AGG_DONE));
@@ -810,16 +1012,19 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     } else if (warp < 4) {
         // warps 2 and 3: no role (warp 2 owns the TMEM allocation)
     } else if (warp < 8) {
-        // feature builders: token t of the chunk
+        // feature builders: token t of the chunk, alternating between two f(k) buffers
         const int t = (warp - 4) * 32 + lane;
         for (int n = 0; n < nchunks; ++n) {
-            const int s = n & 1;
-            if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n >> 1) & 1, abort_flag, SITE_TMA_FULL)) break;
-            if (n > 0 && !wait_bar(BAR(AB_PHIK_FREE), (n - 1) & 1, abort_flag, SITE_PHIK_FREE)) break;
-            build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK, t);
+            const int s = n % S, pb = n & 1;
+            if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
+            if (n >= 2 && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((n >> 1) - 1) & 1, abort_flag,
+                                    SITE_PHIK_FREE))
+                break;
+            build_features<K, false>(sb + CF::A_OFF_RAWK + s * CF::RAW,
+                                     sb + CF::A_OFF_PHIK + pb * CF::PHI, t, 0u);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL));
+            if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
         }
     } else {
         // writer: S^T rows (and z) -> fp32 slot
@@ -869,18 +1074,52 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // ------------------------------------------------------------------------------------------------
 // Scan: within each run of ranges that continue one head's prefix, turn the per-range partial
 // states into inclusive prefixes (slot i = sum of the partial states of ranges <= i in the run).
+// The runs are listed by the host: block (x, r) handles a slice of the elements of run r.
 // ------------------------------------------------------------------------------------------------
-__global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems, int n_c, long long N,
-                                  int G) {
-    const int i = blockIdx.y;
-    if (!has_aggregate(N, G, i, n_c) || continues_prefix(N, G, i, n_c)) return;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= slot_elems) return;
-    float acc = slots[static_cast<size_t>(i) * slot_elems + e];
-    for (int j = i + 1; j < G && continues_prefix(N, G, j, n_c) && has_aggregate(N, G, j, n_c); ++j) {
-        float *p = slots + static_cast<size_t>(j) * slot_elems + e;
-        acc += *p;
-        *p = acc;
+constexpr int kMaxRanges = 256;  // upper bound on G (one range per SM)
+struct ScanRuns {
+    int n;                         // number of runs with more than one range
+    uint16_t start[kMaxRanges];    // first slot of the run
+    uint16_t len[kMaxRanges];      // slots in the run (>= 2)
+};
+
+// Lists the runs of G ranges whose partial states chain into one head's prefix: a run starts at a
+// range with an aggregate that does not continue a prefix and extends over the ranges that do.
+// Single-range runs need no scan and are left out.
+inline ScanRuns make_scan_runs(long long N, int G, int n_c) {
+    ScanRuns runs;
+    runs.n = 0;
+    for (int i = 0; i < G; ++i) {
+        if (!has_aggregate(N, G, i, n_c) || continues_prefix(N, G, i, n_c)) continue;
+        int j = i + 1;
+        while (j < G && continues_prefix(N, G, j, n_c) && has_aggregate(N, G, j, n_c)) ++j;
+        if (j - i >= 2) {
+            runs.start[runs.n] = static_cast<uint16_t>(i);
+            runs.len[runs.n] = static_cast<uint16_t>(j - i);
+            ++runs.n;
+        }
+    }
+    return runs;
+}
+
+__global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems,
+                                  const __grid_constant__ ScanRuns runs) {
+    const int r = blockIdx.y;
+    if (r >= runs.n) return;
+    const int i0 = runs.start[r], len = runs.len[r];
+    const int vec = slot_elems / 4;  // slots are whole float4s
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < vec; e += gridDim.x * blockDim.x) {
+        float4 *p = reinterpret_cast<float4 *>(slots + static_cast<size_t>(i0) * slot_elems) + e;
+        float4 acc = *p;
+        for (int j = 1; j < len; ++j) {
+            p += vec;
+            const float4 x = *p;
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+            *p = acc;
+        }
     }
 }
 

@@ -11,7 +11,7 @@ using namespace based;
 
 int main() {
     long long checked = 0;
-    for (int sms : {1, 2, 7, 148, 152, 160}) {
+    for (int sms : {1, 2, 7, 148, 152, 160, 256}) {
         for (int heads : {1, 2, 3, 5, 16, 64, 96, 256}) {
             for (int T : {1, 64, 127, 128, 129, 300, 1000, 3000, 4096, 16384}) {
                 const int n_c = (T + kChunk - 1) / kChunk;
@@ -32,11 +32,13 @@ int main() {
                 }
                 for (long long g = 0; g < N; ++g)
                     if (covered[g] != 1) { printf("chunk %lld covered %d times\n", g, covered[g]); return 1; }
-                // scan: chains start at slots with an aggregate that do not continue a prefix
-                for (int i = 0; i < G; ++i) {
-                    if (!has_aggregate(N, G, i, n_c) || continues_prefix(N, G, i, n_c)) continue;
-                    for (int j = i + 1; j < G && continues_prefix(N, G, j, n_c) && has_aggregate(N, G, j, n_c); ++j) {
-                        if (hd[j] != hd[j - 1] || hi[j - 1] != lo[j]) { printf("bad chain link\n"); return 1; }
+                // scan over the runs the host lists: slot j takes the chunks of slot j-1
+                const ScanRuns runs = make_scan_runs(N, G, n_c);
+                for (int r = 0; r < runs.n; ++r) {
+                    const int i0 = runs.start[r], len = runs.len[r];
+                    if (len < 2 || i0 + len > G) { printf("bad run\n"); return 1; }
+                    for (int j = i0 + 1; j < i0 + len; ++j) {
+                        if (hd[j] < 0 || hd[j] != hd[j - 1] || hi[j - 1] != lo[j]) { printf("bad chain link\n"); return 1; }
                         lo[j] = lo[j - 1];
                     }
                 }
