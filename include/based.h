@@ -62,7 +62,8 @@ enum {
     BASED_ERR_CUDA = -8,           /* a CUDA runtime/driver call failed (see based_last_cuda_error) */
     BASED_ERR_DEVICE_TIMEOUT = -9, /* a kernel gave up a bounded wait (based_device_status) */
     BASED_ERR_NO_DEVICE = -10,     /* no sm_103 device is current */
-    BASED_ERR_BAD_ARGUMENT = -11   /* any other invalid argument */
+    BASED_ERR_BAD_ARGUMENT = -11,  /* any other invalid argument */
+    BASED_ERR_SCRATCH_LIMIT = -12  /* shape needs more than BASED_NOALLOC_SCRATCH_BYTES of scratch */
 };
 
 /*
@@ -88,6 +89,31 @@ BASED_API size_t based_fwd_workspace_size(int B, int T, int H, int K, int V);
 BASED_API int based_fwd_ws(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
                  int K, int V, float scale, float *o, void *workspace, size_t ws_bytes,
                  based_stream_t stream);
+
+/*
+ * based_fwd_noalloc: based_fwd for callers that may not allocate device memory while they run,
+ * e.g. a serving loop whose device memory is planned up front by its own allocator, or code
+ * that cannot afford the device-wide synchronisation cudaMalloc/cudaFree can cause. The paper
+ * and the kernel-task spec have no counterpart to this entry point: it only changes where the
+ * scratch lives.
+ *   Arguments, layouts, scale and the result are those of based_fwd. Scratch (the per-segment
+ *   partial states) lives in one fixed array of BASED_NOALLOC_SCRATCH_BYTES bytes that is part of
+ *   the library's device image: every GPU that loads the library holds it until process exit.
+ *   The call itself runs no cudaMalloc, cudaFree or other allocating routine.
+ *   - Shapes whose scratch would exceed the array are rejected with BASED_ERR_SCRATCH_LIMIT
+ *     before anything is launched (based_fwd_workspace_size() tells the need; for K = 16,
+ *     V = 128 it is 82,560 bytes per SM, so 16 MiB covers up to 203 SMs).
+ *   - The first call on a device looks up the array's device address (and loads the library's
+ *     device code there if that has not happened yet); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents. No
+ *     scratch element has to start at zero: each call writes every element it reads before
+ *     reading it. Calls that overlap on the GPU (other streams, other threads) race on the array
+ *     and give wrong results: order them (same stream, or events).
+ */
+#define BASED_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+BASED_API int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T,
+                                int H, int K, int V, float scale, float *o, based_stream_t stream);
 
 /*
  * based_fwd_host: the same computation on HOST buffers, end to end. Copies q, k, v to

@@ -37,6 +37,9 @@ def _load():
     L.based_fwd_ws.argtypes = [u16p, u16p, u16p, i, i, i, i, i, ctypes.c_float, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     L.based_fwd_ws.restype = i
+    L.based_fwd_noalloc.argtypes = [u16p, u16p, u16p, i, i, i, i, i, ctypes.c_float,
+                                    ctypes.c_void_p, ctypes.c_void_p]
+    L.based_fwd_noalloc.restype = i
     L.based_fwd_timed.argtypes = [u16p, u16p, u16p, i, i, i, i, i, ctypes.c_float,
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_void_p]
@@ -119,6 +122,26 @@ def based_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional
                                 _scale_arg(scale), out.data_ptr(), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), st.cuda_stream)
     _check(rc, "based_fwd")
+    return out
+
+
+def based_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                      scale: Optional[float] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """based_fwd for callers that may not allocate device memory while they run: the library's
+    scratch is a fixed array of its device image and the caller passes the output buffer. Calls
+    on one device share that array, so calls that overlap on the GPU race; order them."""
+    L = _load()
+    B, T, H, K, V = _shapes(q, k, v)
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and out.is_cuda):
+        raise ValueError("based_fwd_noalloc takes CUDA tensors")
+    if out.dtype != torch.float32 or tuple(out.shape) != (B, T, H, V) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of shape (B,T,H,V)")
+    with torch.cuda.device(q.device):
+        st = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = L.based_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                                 _scale_arg(scale), out.data_ptr(), st.cuda_stream)
+    _check(rc, "based_fwd_noalloc")
     return out
 
 

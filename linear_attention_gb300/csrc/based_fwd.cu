@@ -234,6 +234,30 @@ int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, i
     return launch<8, 128>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
 }
 
+// Scratch of based_fwd_noalloc: a fixed array in the library's device image, so that the entry
+// point never allocates. Its host-side name is only a handle; the device address is looked up per
+// device with cudaGetSymbolAddress.
+__device__ __align__(256) unsigned char g_noalloc_scratch[BASED_NOALLOC_SCRATCH_BYTES];
+
+struct NoAllocState {
+    std::mutex m;
+    void *ptr = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Device address of the scratch array on device `dev` (current), looked up on first use.
+int noalloc_scratch(int dev, void **ptr) {
+    NoAllocState &s = g_noalloc[dev];
+    std::lock_guard<std::mutex> lk(s.m);
+    if (s.ptr == nullptr) {
+        void *p = nullptr;
+        BASED_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+        s.ptr = p;
+    }
+    *ptr = s.ptr;
+    return BASED_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,6 +271,19 @@ int based_fwd_timed(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
                     int K, int V, float scale, float *o, based_stream_t stream, void *ev_begin,
                     void *ev_end) {
     return run(q, k, v, B, T, H, K, V, scale, o, nullptr, 0, true, stream, ev_begin, ev_end);
+}
+
+int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
+                      int K, int V, float scale, float *o, based_stream_t stream) {
+    int rc = check_args(q, k, v, B, T, H, K, V, o);
+    if (rc != BASED_OK) return rc;
+    int dev;
+    if ((rc = current_device(&dev)) != BASED_OK) return rc;
+    const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms);
+    if (p.ws_bytes > BASED_NOALLOC_SCRATCH_BYTES) return BASED_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (p.ws_bytes > 0 && (rc = noalloc_scratch(dev, &scratch)) != BASED_OK) return rc;
+    return run(q, k, v, B, T, H, K, V, scale, o, scratch, p.ws_bytes, false, stream);
 }
 
 int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
@@ -368,6 +405,8 @@ const char *based_strerror(int code) {
         case BASED_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
         case BASED_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
         case BASED_ERR_BAD_ARGUMENT: return "invalid argument";
+        case BASED_ERR_SCRATCH_LIMIT:
+            return "shape needs more scratch than the fixed BASED_NOALLOC_SCRATCH_BYTES array";
         default: return "unknown error code";
     }
 }
