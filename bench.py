@@ -171,6 +171,12 @@ def dist_barrier(world):
         dist.barrier()
 
 
+def job_value(tokens_per_step, steps, elapsed_ms, world):
+    """Whole-job throughput: every rank processes its own replica of the workload, the time is the
+    slowest rank's."""
+    return world * tokens_per_step * steps / (elapsed_ms * 1e-3)
+
+
 def workload_config(w, extra=None):
     cfg = {"workload": f"Based fwd {w.name}: B={w.B} T={w.T} H={w.H} K={w.K} V={w.V}",
            "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
@@ -316,7 +322,7 @@ def run_gpu(args, w, world, rank, local):
 
     ms_per_step = elapsed_ms / args.steps
     tokens_per_step = B * T
-    value = world * tokens_per_step * args.steps / (elapsed_ms * 1e-3)
+    value = job_value(tokens_per_step, args.steps, elapsed_ms, world)
     flops = canonical_flops(B, T, H, K, V)
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
