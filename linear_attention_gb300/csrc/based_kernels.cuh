@@ -215,11 +215,15 @@ __device__ __forceinline__ uint32_t taylor2(uint32_t s_lo, uint32_t s_hi, uint64
 //         1, 0 x 7].
 // K = 8:  block 0 = [x, x_a^2], 1 = [x_a x_{a+1}, x_a x_{a+2}] (mod 8), 2 = [x_a x_{a+3} (mod 8),
 //         x_a x_{a+4} (a<4), 1, 0 x 3].
-// Every unordered pair a < b appears exactly once. With SCALED (the query side) the row is
-// f~(x) = f(sigma x) with the squares halved: x is first multiplied by sig2 = (sigma, sigma),
-// so that f~(q).f(k) = 1 + sigma q.k + sigma^2 (q.k)^2 / 2.
-template <int K, bool SCALED>
-__device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t sig2) {
+// Every unordered pair a < b appears exactly once. x is first multiplied by sig2 and the squares
+// by half2 (bf16 pairs): (1, 1) and (1, 1) give f(k); (sigma, sigma) and (1/2, 1/2) give the
+// query side f~(q) = f(sigma q) with halved squares, so that f~(q).f(k) = 1 + sigma q.k +
+// sigma^2 (q.k)^2 / 2. (Multiplying by 1.0 is exact, so both sides share this one code path.)
+// Out of line: the q and k builders share one copy of the code, which keeps the kernel's
+// instruction-cache footprint small.
+template <int K>
+__device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t sig2,
+                                            uint32_t half2) {
     const uint32_t rb = raw + static_cast<uint32_t>(t) * 32u;
     const uint32_t sw = static_cast<uint32_t>(((t >> 2) & 1) << 4);
     const uint4 lo = ld_shared_v4(rb + sw);
@@ -230,15 +234,12 @@ __device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t
         st_shared_v4(base + (16u ^ sw), p4, p5, p6, p7);
     };
     constexpr uint32_t ONE_ZERO = 0x00003F80u;  // bf16 pair (1.0, 0.0)
-    constexpr uint32_t HALF2 = 0x3F003F00u;     // bf16 pair (0.5, 0.5)
-    auto sq = [&](uint32_t x) { return SCALED ? bmul2(bmul2(x, HALF2), x) : bmul2(x, x); };
+    auto sq = [&](uint32_t x) { return bmul2(bmul2(x, half2), x); };
     if constexpr (K == 16) {
         const uint4 hi = ld_shared_v4(rb + (16u ^ sw));
         uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        if (SCALED) {
 #pragma unroll
-            for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], sig2);
-        }
+        for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], sig2);
         store_blk(0, X[0], X[1], X[2], X[3], X[4], X[5], X[6], X[7]);
         store_blk(1, sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]), sq(X[4]), sq(X[5]), sq(X[6]), sq(X[7]));
 #pragma unroll
@@ -260,10 +261,8 @@ __device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t
                   ONE_ZERO, 0u, 0u, 0u);
     } else {
         uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
-        if (SCALED) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], sig2);
-        }
+        for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], sig2);
         store_blk(0, X[0], X[1], X[2], X[3], sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]));
         uint32_t R1[4], R3[4];
 #pragma unroll
@@ -277,6 +276,8 @@ __device__ __forceinline__ void build_features(uint32_t raw, uint32_t phi, int t
                   bmul2(X[0], X[2]), bmul2(X[1], X[3]), ONE_ZERO, 0u);
     }
 }
+constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
+constexpr uint32_t kBf16Half2 = 0x3F003F00u;  // bf16 pair (0.5, 0.5)
 
 // ------------------------------------------------------------------------------------------------
 // Work partition: the B*H*n_c chunks, ordered head-major, are cut into G contiguous ranges.
@@ -589,9 +590,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t z16[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) z16[j] = 0u;
-#pragma unroll
+            // two key blocks per TMEM round trip; blocks above the diagonal block are zero. The
+            // pair loop is not unrolled (one copy of its body keeps the code small).
+#pragma unroll 1
             for (int kp = 0; kp < 4; kp += 2) {
-                // two key blocks per TMEM round trip; blocks above the diagonal block are zero
                 if (kp <= q4) {
                     uint32_t r0[32], r1[32];
                     tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * kp, r0);
@@ -603,12 +605,12 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const int kb = kp + h;
                         if (kb > q4) break;
                         const uint32_t *r = h ? r1 : r0;
+                        const bool diag = kb == q4;
                         uint32_t packed[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            packed[i] = taylor2(r[2 * i], r[2 * i + 1], C2, C1, ONE);
-                            if (kb == q4) packed[i] &= diag_mask(i);
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            packed[i] = taylor2(r[2 * i], r[2 * i + 1], C2, C1, ONE) &
+                                        (diag ? diag_mask(i) : 0xFFFFFFFFu);
                         // V = 128: A columns [16 kb, 16 kb + 16) overlay s columns already read
                         tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, packed);
                     }
@@ -694,7 +696,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !wait_bar(BAR(FB_PHIQ_FREE), (ro_idx - 1) & 1, abort_flag, SITE_PHIQ_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_BEGIN);
-            build_features<K, true>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, sig2);
+            build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, sig2, kBf16Half2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIQ_FULL));
@@ -707,7 +709,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !wait_bar(BAR(FB_PHIK_FREE), (upd_idx - 1) & 1, abort_flag, SITE_PHIK_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIK_BEGIN);
-            build_features<K, false>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, 0u);
+            build_features<K>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, kBf16One2, kBf16One2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIK_FULL));
@@ -749,31 +751,27 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool warp_has_rows = q4 * 32 <= LAST_ROW;
         constexpr int BATCH = V == 64 ? (CF::NBLK + 1) / 2 : 4;  // blocks per TMEM round trip
 
+        // One block of a state row as bf16: rows r < V are S^T rows; with the z row (V = 64) row V
+        // is z rounded to bf16 and row V + 1 its rounding remainder (z as a hi/lo pair, about 16
+        // significant bits). One code path for both kinds of row keeps the code small.
         auto put_block = [&](uint32_t sbf, int f, const uint32_t *x) {
             const uint32_t blk = sbf + CF::SBF_BLK * f;
-            if (r < V) {
-                st_shared_v4(blk + sw32(r, 0), pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                             pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                             pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                             pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
-                st_shared_v4(blk + sw32(r, 1), pack_bf16x2(__uint_as_float(x[8]), __uint_as_float(x[9])),
-                             pack_bf16x2(__uint_as_float(x[10]), __uint_as_float(x[11])),
-                             pack_bf16x2(__uint_as_float(x[12]), __uint_as_float(x[13])),
-                             pack_bf16x2(__uint_as_float(x[14]), __uint_as_float(x[15])));
-            } else if (CF::ZROW && r == V) {
-                // z as a hi/lo pair of bf16 rows: about 16 significant bits
-                uint32_t hi[8], lw[8];
+            if (r <= LAST_ROW) {
+                uint32_t hi[8];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const float a = __uint_as_float(x[j]), b = __uint_as_float(x[j + 1]);
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-                    hi[j >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
-                    lw[j >> 1] = pack_bf16x2(a - __low2float(h2), b - __high2float(h2));
+                for (int j = 0; j < 8; ++j)
+                    hi[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                st_shared_v4(blk + sw32(r, 0), hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(blk + sw32(r, 1), hi[4], hi[5], hi[6], hi[7]);
+                if (CF::ZROW && r == V) {
+                    uint32_t lw[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        lw[j] = pack_bf16x2(__uint_as_float(x[2 * j]) - __uint_as_float(hi[j] << 16),
+                                            __uint_as_float(x[2 * j + 1]) - __uint_as_float(hi[j] & 0xFFFF0000u));
+                    st_shared_v4(blk + sw32(V + 1, 0), lw[0], lw[1], lw[2], lw[3]);
+                    st_shared_v4(blk + sw32(V + 1, 1), lw[4], lw[5], lw[6], lw[7]);
                 }
-                st_shared_v4(blk + sw32(V, 0), hi[0], hi[1], hi[2], hi[3]);
-                st_shared_v4(blk + sw32(V, 1), hi[4], hi[5], hi[6], hi[7]);
-                st_shared_v4(blk + sw32(V + 1, 0), lw[0], lw[1], lw[2], lw[3]);
-                st_shared_v4(blk + sw32(V + 1, 1), lw[4], lw[5], lw[6], lw[7]);
             }
         };
         auto put_z = [&](uint32_t sbf, int p, float z) {
@@ -802,8 +800,9 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 zb = __uint_as_float(b);
             }
             if (warp_has_rows) {
-                // BATCH feature blocks per TMEM round trip; S^T is released after the last load
-#pragma unroll
+                // BATCH feature blocks per TMEM round trip; S^T is released after the last load.
+                // The batch loop is not unrolled (one copy of its body keeps the code small).
+#pragma unroll 1
                 for (int f0 = 0; f0 < CF::NBLK; f0 += BATCH) {
                     uint32_t x[BATCH][16];
 #pragma unroll
@@ -1020,8 +1019,8 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (n >= 2 && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((n >> 1) - 1) & 1, abort_flag,
                                     SITE_PHIK_FREE))
                 break;
-            build_features<K, false>(sb + CF::A_OFF_RAWK + s * CF::RAW,
-                                     sb + CF::A_OFF_PHIK + pb * CF::PHI, t, 0u);
+            build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
+                              kBf16One2, kBf16One2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
