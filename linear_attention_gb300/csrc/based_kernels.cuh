@@ -590,36 +590,38 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t z16[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) z16[j] = 0u;
-            // two key blocks per TMEM round trip; blocks above the diagonal block are zero. The
-            // pair loop is not unrolled (one copy of its body keeps the code small).
+            // Key blocks 0..q4 of 32 keys (blocks above the diagonal block are zero), one per step
+            // with the load of the next one in flight. Rolled by two blocks (one copy of the body
+            // keeps the code small).
+            uint32_t ra[32], rb[32];
+            tmem_ld_x32(tmem + lo + CF::TM_SC, ra);
+            auto weights = [&](int kb, uint32_t (&r)[32]) {
+                const bool diag = kb == q4;
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i] = taylor2(r[2 * i], r[2 * i + 1], C2, C1, ONE) &
+                                (diag ? diag_mask(i) : 0xFFFFFFFFu);
+                // V = 128: A columns [16 kb, 16 kb + 16) overlay s columns already read
+                tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, packed);
+            };
 #pragma unroll 1
-            for (int kp = 0; kp < 4; kp += 2) {
-                if (kp <= q4) {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * kp, r0);
-                    if (kp + 1 <= q4) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kp + 1), r1);
-                    tmem_wait_ld();
-                    if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kp == 0 ? TE_POLY_LD0 : TE_POLY_LD1);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kb = kp + h;
-                        if (kb > q4) break;
-                        const uint32_t *r = h ? r1 : r0;
-                        const bool diag = kb == q4;
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            packed[i] = taylor2(r[2 * i], r[2 * i + 1], C2, C1, ONE) &
-                                        (diag ? diag_mask(i) : 0xFFFFFFFFu);
-                        // V = 128: A columns [16 kb, 16 kb + 16) overlay s columns already read
-                        tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, packed);
-                    }
-                    if (!FAST && kp + 1 > q4) tmem_st_x16(tmem + lo + CF::TM_A + 16 * (kp + 1), z16);
-                    if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kp == 0 ? TE_POLY_ST0 : TE_POLY_ST1);
-                } else if (!FAST) {
-                    tmem_st_x16(tmem + lo + CF::TM_A + 16 * kp, z16);
-                    tmem_st_x16(tmem + lo + CF::TM_A + 16 * (kp + 1), z16);
+            for (int kb = 0; kb <= q4; kb += 2) {
+                const bool two = kb + 1 <= q4;
+                if (two) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb + 1), rb);
+                tmem_wait_ld_dep(ra);
+                if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kb == 0 ? TE_POLY_LD0 : TE_POLY_LD1);
+                weights(kb, ra);
+                if (two) {
+                    if (kb + 2 <= q4) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb + 2), ra);
+                    tmem_wait_ld_dep(rb);
+                    weights(kb + 1, rb);
                 }
+            }
+            if constexpr (!FAST) {
+                // V = 128: A overlays s, so the blocks above the diagonal block are cleared each time
+#pragma unroll 1
+                for (int kb = q4 + 1; kb < 4; ++kb) tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, z16);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -800,24 +802,28 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 zb = __uint_as_float(b);
             }
             if (warp_has_rows) {
-                // BATCH feature blocks per TMEM round trip; S^T is released after the last load.
-                // The batch loop is not unrolled (one copy of its body keeps the code small).
+                // One feature block per step, the load of the next one in flight while the current
+                // one is converted; S^T is released once its last block is in registers. Rolled by
+                // two blocks (one copy of the body keeps the code small).
+                uint32_t xa[16], xb[16];
+                tmem_ld_x16(tmem + lo + CF::TM_S, xa);
 #pragma unroll 1
-                for (int f0 = 0; f0 < CF::NBLK; f0 += BATCH) {
-                    uint32_t x[BATCH][16];
-#pragma unroll
-                    for (int f = 0; f < BATCH; ++f)
-                        if (f0 + f < CF::NBLK) tmem_ld_x16(tmem + lo + CF::TM_S + 16 * (f0 + f), x[f]);
-                    tmem_wait_ld();
-                    if (f0 + BATCH >= CF::NBLK) {
+                for (int f = 0; f < CF::NBLK; f += 2) {
+                    const bool two = f + 1 < CF::NBLK;
+                    if (two) tmem_ld_x16(tmem + lo + CF::TM_S + 16 * (f + 1), xb);
+                    tmem_wait_ld_dep(xa);
+                    reg_fence(xb);
+                    if (f + 2 >= CF::NBLK) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(BAR(FB_CONV_READ));  // S^T may change now
                         if (warp == 12 && lane == 0) BASED_TRACE_EV(n, TE_CONV_READ);
                     }
-#pragma unroll
-                    for (int f = 0; f < BATCH; ++f)
-                        if (f0 + f < CF::NBLK) put_block(sbf, f0 + f, x[f]);
+                    put_block(sbf, f, xa);
+                    if (two) {
+                        if (f + 2 < CF::NBLK) tmem_ld_x16(tmem + lo + CF::TM_S + 16 * (f + 2), xa);
+                        put_block(sbf, f + 1, xb);
+                    }
                 }
             } else {
                 tc_fence_before();
