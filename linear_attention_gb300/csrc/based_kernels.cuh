@@ -68,21 +68,33 @@ __device__ __forceinline__ void record_timeout(uint32_t site) {
     atomicOr(&g_status, 1u);
 }
 
+// Gives up a wait: aborts the CTA and records the site (rare path, kept out of line).
+__device__ __noinline__ void give_up_wait(volatile int *abort_flag, uint32_t site) {
+    if (abort_flag != nullptr) *abort_flag = 1;
+    record_timeout(site);
+}
+
 // Bounded mbarrier wait. Returns false if the CTA aborted or the wait ran out (then it aborts
 // the CTA and records the site). Never spins longer than the limit.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                      uint32_t site, uint64_t limit_ns = kWaitLimitNs) {
+__device__ __forceinline__ bool wait_bar_inline(uint32_t bar, uint32_t parity,
+                                                volatile int *abort_flag, uint32_t site,
+                                                uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if ((it & 15u) == 0u && global_timer_ns() - t0 > limit_ns) {
-            if (abort_flag != nullptr) *abort_flag = 1;
-            record_timeout(site);
+            give_up_wait(abort_flag, site);
             return false;
         }
     }
+}
+// The same wait as an out-of-line call: every role shares one copy of the loop, which keeps the
+// kernel's code (and its instruction-cache footprint) small.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                      uint32_t site, uint64_t limit_ns = kWaitLimitNs) {
+    return wait_bar_inline(bar, parity, abort_flag, site, limit_ns);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -342,7 +354,7 @@ struct Cursor {
 enum FwdBar {
     FB_TMA_FULL0 = 0, FB_STAGE_FREE0 = 3, FB_S_FULL = 6, FB_A_FULL, FB_O_FULL0, FB_O_FULL1,
     FB_O_FREE0, FB_O_FREE1, FB_AV_DONE, FB_PHIQ_FULL, FB_PHIQ_FREE, FB_PHIK_FULL, FB_PHIK_FREE,
-    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_COUNT
+    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_DRAIN_B, FB_AV_DONE1, FB_COUNT
 };
 
 template <int K, int V>
@@ -371,7 +383,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ---- set-up: barriers, constant tiles, TMEM -------------------------------------------------
     if (threadIdx.x == 0) {
         // arrivals per phase: 1 = producer / commit, 4 = one elected lane per warp of a group
-        const uint32_t counts[FB_COUNT] = {1, 1, 1, 1, 1, 1, 1, 4, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, 4, 4, 1};
+        // STAGE_FREE: one commit from each MMA issuer
+        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, 4, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, 4, 4, 1, 1, 1};
         for (int i = 0; i < FB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -437,104 +450,123 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                  SITE_DRAIN, kDrainLimitNs);
             }
         }
-    } else if (warp == 1) {
-        // ================================ MMA issuer ===========================================
+    } else if (warp == 1 || warp == 3) {
+        // ============================== MMA issuers ============================================
+        // Two threads issue MMAs, so that neither stream waits on the other's inputs: warp 1 the
+        // intra-chunk products (s = q k^T, O = A [v | 1]), warp 3 the state products (S^T +=
+        // [v | 1]^T f(k), O += f~(q) [S | z]). Each thread's MMAs run in its issue order; the
+        // read-out accumulates into the O tile of a chunk only after AV_DONE shows that
+        // A [v | 1] (which initialises it) has completed.
         if (lane == 0) {
             const uint32_t t_s = tmem + CF::TM_S, t_sc = tmem + CF::TM_SC, t_a = tmem + CF::TM_A,
                            t_z = tmem + CF::TM_Z;
             const uint32_t t_o0 = tmem + CF::TM_O0, t_o1 = tmem + CF::TM_O1;
-            constexpr uint32_t ID_QK = idesc_bf16_f32(128, 128, 0, 0);
-            constexpr uint32_t ID_AV = idesc_bf16_f32(128, FAST ? CF::NO : V, 0, 1);
-            constexpr uint32_t ID_RS = idesc_bf16_f32(128, 16, 0, 0);
-            constexpr uint32_t ID_RO = idesc_bf16_f32(128, CF::NO, 0, 0);
-            constexpr uint32_t ID_UPD = idesc_bf16_f32(128, CF::PP, 1, 1);
-            constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
             // Operand descriptors, computed once: per k-step and per stage only the start address
             // advances. Raw q/k tiles are K-major SW32; v_c is an MN-major SW128 operand whose
             // second 64-wide block is the ones block (V = 64, LBO depends on the stage) or the
             // upper half of v_c (V = 128).
-            const uint64_t d_q = smem_desc(sb + CF::OFF_RAWQ, 16, 256, LAYOUT_SW32);
-            const uint64_t d_k = smem_desc(sb + CF::OFF_RAWK, 16, 256, LAYOUT_SW32);
             auto va_desc = [&](int s) {  // k-step 0 of stage s
                 const uint32_t lbo = CF::ZROW ? CF::OFF_ONES - CF::OFF_V - s * CF::VT : 16384u;
                 return smem_desc(sb + CF::OFF_V + s * CF::VT, lbo, 1024, LAYOUT_SW128);
             };
             const uint64_t d_va0 = va_desc(0), d_va1 = va_desc(1), d_va2 = va_desc(CF::NST > 2 ? 2 : 1);
-            const uint64_t d_sbf0 = smem_desc(sb + CF::OFF_SBF, 16, 256, LAYOUT_SW32);
-            const uint64_t d_sbf1 = smem_desc(sb + CF::OFF_SBF + (CF::NSBF - 1) * CF::SBF, 16, 256, LAYOUT_SW32);
-            const uint64_t d_phik = smem_desc(sb + CF::OFF_PHIK, 4096, 256, LAYOUT_SW32);
-            const uint64_t d_phiq = smem_desc(sb + CF::OFF_PHIQ, 16, 256, LAYOUT_SW32);
             const uint64_t d_zones = smem_desc(sb + CF::OFF_ZONES, 16, 256, LAYOUT_SW32);
-
-            int ro_idx = 0, upd_idx = 0;
-            bool ok = wait_bar(BAR(FB_TMA_FULL0), 0, abort_flag, SITE_TMA_FULL);
-            if (ok) {
-                tc_fence_after();
-                mma_ss(t_sc, d_q, d_k, ID_QK, 0);
-                mma_commit(BAR(FB_S_FULL));
-            }
-            auto issue_ro = [&](uint32_t t_out) -> bool {
-                // O += f~(q_c) [S | z_hi z_lo]
-                if (!wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)) return false;
-                if (!wait_bar(BAR(FB_SBF_FULL), ro_idx & 1, abort_flag, SITE_SBF_FULL)) return false;
-                tc_fence_after();
-                const uint64_t db = (ro_idx & 1) ? d_sbf1 : d_sbf0;
-#pragma unroll
-                for (int f = 0; f < CF::NBLK; ++f)
-                    mma_ss(t_out, dadd(d_phiq, 4096 * f), dadd(db, CF::SBF_BLK * f), ID_RO, 1);
-                mma_commit(BAR(FB_PHIQ_FREE));
-                ++ro_idx;
-                return true;
-            };
             Cursor cu;
             cu.init(g0, nchunks, n_c, H);
-            for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
-                const int s = n % CF::NST;
-                const int ob = FAST ? (n & 1) : 0;
-                const uint64_t d_va = s == 0 ? d_va0 : (s == 1 ? d_va1 : d_va2);
-                const uint32_t t_out = ob ? t_o1 : t_o0;
-                if (!(ok = wait_bar(BAR(FB_A_FULL), n & 1, abort_flag, SITE_A_FULL))) break;
-                BASED_TRACE_EV(n, TE_A_READY);
-                if (FAST ? (n >= 2) : (n >= 1)) {
-                    const uint32_t par = FAST ? (((n >> 1) - 1) & 1) : ((n - 1) & 1);
-                    if (!(ok = wait_bar(BAR(FB_O_FREE0 + ob), par, abort_flag, SITE_O_FREE))) break;
-                }
-                tc_fence_after();
-                // O = A [v_c | 1]: numerators and rowsum A (V = 64: one MMA per 16 keys over the
-                // v block and the ones block; V = 128: a separate 16-column MMA for the rowsum)
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    mma_ts(t_out, t_a + 8 * j, v_step<CF::ZROW>(d_va, j), ID_AV, j > 0);
-                BASED_TRACE_EV(n, TE_AV_ISSUED);
-                if constexpr (!FAST) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) mma_ts(t_out + V, t_a + 8 * j, d_zones, ID_RS, j > 0);
-                    mma_commit(BAR(FB_AV_DONE));
-                    if (cu.has_ro() && !(ok = issue_ro(t_out))) break;
-                    mma_commit(BAR(FB_O_FULL0));
-                    BASED_TRACE_EV(n, TE_RO_ISSUED);
-                    // the next s overwrites A (same TMEM columns): wait until A has been read
-                    if (!(ok = wait_bar(BAR(FB_AV_DONE), n & 1, abort_flag, SITE_AV_DONE))) break;
-                }
-                if (n + 1 < nchunks) {
-                    const int s1 = (n + 1) % CF::NST;
-                    if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s1), ((n + 1) / CF::NST) & 1, abort_flag,
-                                        SITE_TMA_FULL)))
-                        break;
+            if (warp == 1) {
+                // ---- intra-chunk stream: QK(0); per chunk AV(n), QK(n + 1) ----
+                constexpr uint32_t ID_QK = idesc_bf16_f32(128, 128, 0, 0);
+                constexpr uint32_t ID_AV = idesc_bf16_f32(128, FAST ? CF::NO : V, 0, 1);
+                constexpr uint32_t ID_RS = idesc_bf16_f32(128, 16, 0, 0);
+                const uint64_t d_q = smem_desc(sb + CF::OFF_RAWQ, 16, 256, LAYOUT_SW32);
+                const uint64_t d_k = smem_desc(sb + CF::OFF_RAWK, 16, 256, LAYOUT_SW32);
+                bool ok = wait_bar(BAR(FB_TMA_FULL0), 0, abort_flag, SITE_TMA_FULL);
+                if (ok) {
                     tc_fence_after();
-                    mma_ss(t_sc, dadd(d_q, s1 * CF::RAW), dadd(d_k, s1 * CF::RAW), ID_QK, 0);
+                    mma_ss(t_sc, d_q, d_k, ID_QK, 0);
                     mma_commit(BAR(FB_S_FULL));
-                    BASED_TRACE_EV(n, TE_QK_ISSUED);
                 }
-                if (cu.has_upd()) {
+                for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
+                    const int s = n % CF::NST;
+                    const int ob = FAST ? (n & 1) : 0;
+                    const uint64_t d_va = s == 0 ? d_va0 : (s == 1 ? d_va1 : d_va2);
+                    const uint32_t t_out = ob ? t_o1 : t_o0;
+                    if (!(ok = wait_bar(BAR(FB_A_FULL), n & 1, abort_flag, SITE_A_FULL))) break;
+                    BASED_TRACE_EV(n, TE_A_READY);
+                    if (FAST ? (n >= 2) : (n >= 1)) {
+                        const uint32_t par = FAST ? (((n >> 1) - 1) & 1) : ((n - 1) & 1);
+                        if (!(ok = wait_bar(BAR(FB_O_FREE0 + ob), par, abort_flag, SITE_O_FREE))) break;
+                    }
+                    tc_fence_after();
+                    // O = A [v_c | 1]: numerators and rowsum A (V = 64: one MMA per 16 keys over
+                    // the v block and the ones block; V = 128: a separate 16-column MMA for the
+                    // rowsum)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        mma_ts(t_out, t_a + 8 * j, v_step<CF::ZROW>(d_va, j), ID_AV, j > 0);
+                    if constexpr (!FAST) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) mma_ts(t_out + V, t_a + 8 * j, d_zones, ID_RS, j > 0);
+                    }
+                    // one AV_DONE barrier per O buffer (V = 64), so that this stream, which may run a
+                    // chunk ahead, never completes two phases of a barrier the other still waits on
+                    mma_commit(BAR(ob ? FB_AV_DONE1 : FB_AV_DONE));
+                    if (!cu.has_ro()) mma_commit(BAR(FB_O_FULL0 + ob));  // no read-out follows
+                    mma_commit(BAR(FB_STAGE_FREE0 + s));                  // QK(n) and AV(n) read it
+                    BASED_TRACE_EV(n, TE_AV_ISSUED);
+                    if (n + 1 < nchunks) {
+                        if constexpr (!FAST) {
+                            // the next s overwrites A (same TMEM columns): wait until A was read
+                            if (!(ok = wait_bar(BAR(FB_AV_DONE), n & 1, abort_flag, SITE_AV_DONE))) break;
+                        }
+                        const int s1 = (n + 1) % CF::NST;
+                        if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s1), ((n + 1) / CF::NST) & 1, abort_flag,
+                                          SITE_TMA_FULL)))
+                            break;
+                        tc_fence_after();
+                        mma_ss(t_sc, dadd(d_q, s1 * CF::RAW), dadd(d_k, s1 * CF::RAW), ID_QK, 0);
+                        mma_commit(BAR(FB_S_FULL));
+                        BASED_TRACE_EV(n, TE_QK_ISSUED);
+                    }
+                }
+                // every MMA issued must finish before TMEM is released
+                mma_commit(BAR(FB_DRAIN));
+                wait_bar(BAR(FB_DRAIN), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
+            } else {
+                // ---- state stream: per chunk UPD(n) and RO(n) ----
+                constexpr uint32_t ID_RO = idesc_bf16_f32(128, CF::NO, 0, 0);
+                constexpr uint32_t ID_UPD = idesc_bf16_f32(128, CF::PP, 1, 1);
+                constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
+                const uint64_t d_sbf0 = smem_desc(sb + CF::OFF_SBF, 16, 256, LAYOUT_SW32);
+                const uint64_t d_sbf1 = smem_desc(sb + CF::OFF_SBF + (CF::NSBF - 1) * CF::SBF, 16, 256, LAYOUT_SW32);
+                const uint64_t d_phik = smem_desc(sb + CF::OFF_PHIK, 4096, 256, LAYOUT_SW32);
+                const uint64_t d_phiq = smem_desc(sb + CF::OFF_PHIQ, 16, 256, LAYOUT_SW32);
+                int ro_idx = 0, upd_idx = 0;
+                bool ok = true;
+                auto issue_ro = [&](int n, uint32_t t_out) -> bool {
+                    // O += f~(q_c) [S | z_hi z_lo], after O = A [v_c | 1] has completed
+                    if (!wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)) return false;
+                    if (!wait_bar(BAR(FB_SBF_FULL), ro_idx & 1, abort_flag, SITE_SBF_FULL)) return false;
+                    const int ob = FAST ? (n & 1) : 0;
+                    const uint32_t avp = FAST ? ((n >> 1) & 1) : (n & 1);
+                    if (!wait_bar(BAR(ob ? FB_AV_DONE1 : FB_AV_DONE), avp, abort_flag, SITE_AV_DONE))
+                        return false;
+                    tc_fence_after();
+                    const uint64_t db = (ro_idx & 1) ? d_sbf1 : d_sbf0;
+#pragma unroll
+                    for (int f = 0; f < CF::NBLK; ++f)
+                        mma_ss(t_out, dadd(d_phiq, 4096 * f), dadd(db, CF::SBF_BLK * f), ID_RO, 1);
+                    mma_commit(BAR(FB_PHIQ_FREE));
+                    ++ro_idx;
+                    return true;
+                };
+                auto issue_upd = [&](int n, uint64_t d_va) -> bool {
                     // S^T += [v_c | 1]^T f(k_c)  (z as row 64, or via the z MMAs)
-                    if (!(ok = wait_bar(BAR(FB_PHIK_FULL), upd_idx & 1, abort_flag, SITE_PHIK_FULL)))
-                        break;
+                    if (!wait_bar(BAR(FB_PHIK_FULL), upd_idx & 1, abort_flag, SITE_PHIK_FULL)) return false;
                     if (cu.upd_acc()) {
                         // the previous conversion must have read S^T before it changes
                         const int r = FAST ? ro_idx : ro_idx - 1;
-                        if (!(ok = wait_bar(BAR(FB_CONV_READ), r & 1, abort_flag, SITE_CONV_READ)))
-                            break;
+                        if (!wait_bar(BAR(FB_CONV_READ), r & 1, abort_flag, SITE_CONV_READ)) return false;
                     }
                     tc_fence_after();
 #pragma unroll
@@ -551,20 +583,30 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_commit(BAR(FB_PHIK_FREE));
                     BASED_TRACE_EV(n, TE_UPD_ISSUED);
                     ++upd_idx;
+                    return true;
+                };
+                for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
+                    const int s = n % CF::NST;
+                    const int ob = FAST ? (n & 1) : 0;
+                    const uint64_t d_va = s == 0 ? d_va0 : (s == 1 ? d_va1 : d_va2);
+                    const uint32_t t_out = ob ? t_o1 : t_o0;
+                    // V = 64 updates first (double-buffered state operand); V = 128 reads out
+                    // first, so that the single state operand is consumed before it is rewritten
+                    if (FAST && cu.has_upd() && !(ok = issue_upd(n, d_va))) break;
+                    if (cu.has_ro()) {
+                        if (!(ok = issue_ro(n, t_out))) break;
+                        mma_commit(BAR(FB_O_FULL0 + ob));
+                        BASED_TRACE_EV(n, TE_RO_ISSUED);
+                    }
+                    if (!FAST && cu.has_upd() && !(ok = issue_upd(n, d_va))) break;
+                    mma_commit(BAR(FB_STAGE_FREE0 + s));  // UPD(n) read v_c; f(k), f~(q) are built
                 }
-                if constexpr (FAST) {
-                    if (cu.has_ro() && !(ok = issue_ro(t_out))) break;
-                    mma_commit(BAR(FB_O_FULL0 + ob));
-                    BASED_TRACE_EV(n, TE_RO_ISSUED);
-                }
-                mma_commit(BAR(FB_STAGE_FREE0 + s));
+                mma_commit(BAR(FB_DRAIN_B));
+                wait_bar(BAR(FB_DRAIN_B), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
             }
-            // every MMA issued must finish before TMEM is released
-            mma_commit(BAR(FB_DRAIN));
-            wait_bar(BAR(FB_DRAIN), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
         }
-    } else if (warp < 4) {
-        // warps 2 and 3: no role (warp 2 owns the TMEM allocation)
+    } else if (warp == 2) {
+        // warp 2: no role besides owning the TMEM allocation
     } else if (warp < 8) {
         // ======================= Taylor weights: A = poly(s), causal mask =======================
         const int q4 = warp & 3;
