@@ -141,7 +141,7 @@ struct Cfg {
     static constexpr int SBF = NBLK * SBF_BLK;
     static constexpr int NSBF = FAST ? 2 : 1;
     // q/k/v stages in flight: as many as fit (loads are issued NST - 1 chunks ahead)
-    static constexpr int NST = (K == 16 && V == 128) ? 2 : 3;
+    static constexpr int NST = (K == 16) ? 2 : 3;
     static constexpr int OFF_RAWQ = 0;
     static constexpr int OFF_RAWK = OFF_RAWQ + NST * RAW;
     static constexpr int OFF_V = OFF_RAWK + NST * RAW;
@@ -154,8 +154,11 @@ struct Cfg {
     static constexpr int OFF_ZONES = align_up(OFF_SBF + NSBF * SBF, 1024);
     // output staging for TMA stores: 128 rows x 32 fp32 (SW128), one quarter/half of a tile
     static constexpr int OST = kChunk * 128;
+    // two staging buffers where they fit, so that a piece never waits for the previous one's
+    // store to have left shared memory
+    static constexpr int NOST = (K == 16 && V == 128) ? 1 : 2;
     static constexpr int OFF_OST = OFF_ZONES + 1024;
-    static constexpr int OFF_BAR = OFF_OST + OST;
+    static constexpr int OFF_BAR = OFF_OST + NOST * OST;
     static constexpr int SMEM_FWD = OFF_BAR + 256 + 1024;  // + alignment slack
     // The z MMA reads 8 feature blocks (32 KB) from the phi(k) tile start; they must be inside
     // the allocation even when the tile has fewer blocks (their rows of D are never read).
@@ -684,7 +687,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // 32-column pieces (128 rows x 128 B, SW128) by TMA stores, so that the output traffic
         // never occupies the load/store path the TMEM accesses of the other roles use. Rows past T
         // are clipped by the tensor map.
-        const uint32_t ost = sb + CF::OFF_OST;
+        int piece = 0;  // output pieces staged so far (selects the staging buffer)
         auto epilogue = [&](int m, int eb, int eh, int et0) -> bool {
             const int ob = FAST ? (m & 1) : 0;
             const uint32_t par = FAST ? ((m >> 1) & 1) : (m & 1);
@@ -716,7 +719,13 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
                 const uint32_t *r = (p & 1) ? r1 : r0;
-                if (t == 0) bulk_wait_group_read<0>();  // previous piece has left the buffer
+                const uint32_t ost = sb + CF::OFF_OST + (piece % CF::NOST) * CF::OST;
+                ++piece;
+                // the store that last used this buffer has read it
+                if (t == 0) {
+                    if constexpr (CF::NOST == 2) bulk_wait_group_read<1>();
+                    else bulk_wait_group_read<0>();
+                }
                 named_bar_sync(1, 128);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
