@@ -50,9 +50,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// (dim0, H, T, B) tensor of 2-byte (bf16) or 4-byte (fp32) elements with a (box0, 1, 128, 1) box.
+// (dim0, H, T, B) tensor of 2-byte (bf16) or 4-byte (fp32) elements with a
+// (box0, 1, box_rows, 1) box.
 int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, int box0,
-             CUtensorMapSwizzle swz, bool fp32 = false) {
+             CUtensorMapSwizzle swz, bool fp32 = false, int box_rows = kChunk) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) {
         snprintf(tl_cuda_error, sizeof(tl_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -64,7 +65,7 @@ int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, in
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d0) * es,
                                    static_cast<cuuint64_t>(H) * d0 * es,
                                    static_cast<cuuint64_t>(T) * H * d0 * es};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), 1, static_cast<cuuint32_t>(kChunk), 1};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), 1, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                      const_cast<void *>(base), dims,
@@ -179,7 +180,8 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != BASED_OK) return rc;
-    if ((rc = make_map(&mo, o, V, B, T, H, 32, CU_TENSOR_MAP_SWIZZLE_128B, true)) != BASED_OK) return rc;
+    if ((rc = make_map(&mo, o, V, B, T, H, 32, CU_TENSOR_MAP_SWIZZLE_128B, true, CF::EPI_ROWS)) != BASED_OK)
+        return rc;
     if (p.need_agg) {
         based_agg_kernel<K, V><<<p.G, kAggThreads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.N, p.G);
         BASED_CUDA(cudaGetLastError());

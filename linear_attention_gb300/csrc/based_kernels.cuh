@@ -157,6 +157,9 @@ struct Cfg {
     // two staging buffers where they fit, so that a piece never waits for the previous one's
     // store to have left shared memory
     static constexpr int NOST = (K == 16 && V == 128) ? 1 : 2;
+    // rows of one output TMA box: with a single staging buffer every epilogue warp stores its own
+    // 32 rows (no cross-warp barrier); with two, one thread stores all 128 rows of a piece
+    static constexpr int EPI_ROWS = NOST == 1 ? 32 : 128;
     static constexpr int OFF_OST = OFF_ZONES + 1024;
     static constexpr int OFF_BAR = OFF_OST + NOST * OST;
     static constexpr int SMEM_FWD = OFF_BAR + 256 + 1024;  // + alignment slack
@@ -683,10 +686,12 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         int ro_idx = 0, upd_idx = 0;
         bool ok = true;
 
-        // Output tile: o = O_num / (O_den + 1e-6), written through a 16 KB staging buffer as
-        // 32-column pieces (128 rows x 128 B, SW128) by TMA stores, so that the output traffic
-        // never occupies the load/store path the TMEM accesses of the other roles use. Rows past T
-        // are clipped by the tensor map.
+        // Output tile: o = O_num / (O_den + 1e-6), written through staging buffers as 32-column
+        // pieces (SW128) by TMA stores, so that the output traffic never occupies the load/store
+        // path the TMEM accesses of the other roles use. Either each warp stages and stores its
+        // own 32 rows (EPI_ROWS = 32: the four warps never wait for each other), or the four
+        // warps meet at a named barrier and one thread stores the 128-row piece (fewer stores).
+        // Rows past T are clipped by the tensor map; a box that starts past T is not issued.
         int piece = 0;  // output pieces staged so far (selects the staging buffer)
         auto epilogue = [&](int m, int eb, int eh, int et0) -> bool {
             const int ob = FAST ? (m & 1) : 0;
@@ -719,26 +724,36 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
                 const uint32_t *r = (p & 1) ? r1 : r0;
-                const uint32_t ost = sb + CF::OFF_OST + (piece % CF::NOST) * CF::OST;
+                constexpr bool WARP_BOX = CF::EPI_ROWS == 32;
+                const uint32_t ost = sb + CF::OFF_OST + (piece % CF::NOST) * CF::OST + q4 * 4096;
                 ++piece;
                 // the store that last used this buffer has read it
-                if (t == 0) {
+                if (WARP_BOX ? lane == 0 : t == 0) {
                     if constexpr (CF::NOST == 2) bulk_wait_group_read<1>();
                     else bulk_wait_group_read<0>();
                 }
-                named_bar_sync(1, 128);
+                if (WARP_BOX) __syncwarp();
+                else named_bar_sync(1, 128);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    st_shared_v4(ost + static_cast<uint32_t>(t) * 128u + ((c ^ (t & 7)) << 4),
+                    st_shared_v4(ost + static_cast<uint32_t>(lane) * 128u + ((c ^ (lane & 7)) << 4),
                                  __float_as_uint(__uint_as_float(r[4 * c]) * inv),
                                  __float_as_uint(__uint_as_float(r[4 * c + 1]) * inv),
                                  __float_as_uint(__uint_as_float(r[4 * c + 2]) * inv),
                                  __float_as_uint(__uint_as_float(r[4 * c + 3]) * inv));
                 fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (t == 0) {
-                    tma_store_4d(&tm_o, ost, 32 * p, eh, et0, eb);
-                    bulk_commit_group();
+                if (WARP_BOX) {
+                    __syncwarp();
+                    if (lane == 0 && et0 + 32 * q4 < T) {
+                        tma_store_4d(&tm_o, ost, 32 * p, eh, et0 + 32 * q4, eb);
+                        bulk_commit_group();
+                    }
+                } else {
+                    named_bar_sync(1, 128);
+                    if (t == 0) {
+                        tma_store_4d(&tm_o, ost - q4 * 4096, 32 * p, eh, et0, eb);
+                        bulk_commit_group();
+                    }
                 }
             }
             if (warp == 11 && lane == 0) BASED_TRACE_EV(m, TE_EPI_END);
@@ -794,7 +809,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             pt0 = cu.t0();
         }
         if (ok) epilogue(nchunks - 1, pb, ph, pt0);
-        if (t == 0) bulk_wait_group_all();  // the staging buffer must outlive the last store
+        // the staging buffers must outlive the last store
+        if (CF::EPI_ROWS == 32 ? lane == 0 : t == 0) bulk_wait_group_all();
     } else {
         // ============== state conversion: S^T (fp32, TMEM) -> bf16 operand [S | z_hi z_lo] =====
         const int q4 = warp & 3;
