@@ -25,7 +25,6 @@ namespace based {
 constexpr int kChunk = 128;            // rows per chunk = MMA M
 constexpr int kFwdThreads = 512;       // 4 warpgroups
 constexpr int kAggThreads = 384;       // 3 warpgroups
-constexpr int kAggStages = 3;          // k/v stages of the aggregate kernel
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after 1 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // drain of in-flight copies after an abort
 
@@ -117,7 +116,10 @@ struct Cfg {
     static constexpr bool ZROW = (V == 64);
     static constexpr bool FAST = (V == 64);
     static constexpr int NO = V + 16;        // O columns: V numerators, den (rowsum + z_hi), z_lo
-    static constexpr int SROWS = V + 1;      // rows of a stored state: V rows of S^T + z
+    // A stored state (aggregate slot) is feature-major: element (feature c, row r) at
+    // c * SROWS + r, rows r < V of S^T and row V = z, so that the threads of a warp (consecutive
+    // rows) access consecutive floats.
+    static constexpr int SROWS = V + 1;
     static constexpr int SLOT = SROWS * PP;  // floats per stored state
 
     // TMEM columns (forward kernel)
@@ -168,11 +170,14 @@ struct Cfg {
     static_assert(ZROW || OFF_PHIK + 8 * 4096 <= OFF_BAR, "z MMA window leaves shared memory");
     static_assert(SMEM_FWD <= 232448, "shared memory budget");
 
-    // Shared memory (aggregate kernel): two phi(k) buffers, kAggStages k/v stages.
+    // Shared memory (aggregate kernel): two phi(k) buffers and as many k/v stages as fit (at
+    // most 8), so that the loads run far enough ahead to hide the memory latency.
+    static constexpr int A_NST_FIT = (232448 - 1024 - 256 - 1024 - 2048 - align_up(2 * PHI, 1024)) / (RAW + VT);
+    static constexpr int A_NST = A_NST_FIT < 8 ? A_NST_FIT : 8;
     static constexpr int A_OFF_PHIK = 0;
     static constexpr int A_OFF_RAWK = align_up(2 * PHI, 1024);
-    static constexpr int A_OFF_V = A_OFF_RAWK + kAggStages * RAW;
-    static constexpr int A_OFF_ONES = A_OFF_V + kAggStages * VT;
+    static constexpr int A_OFF_V = A_OFF_RAWK + A_NST * RAW;
+    static constexpr int A_OFF_ONES = A_OFF_V + A_NST * VT;
     static constexpr int A_OFF_ZONES = align_up(A_OFF_ONES + ONES, 1024);
     static constexpr int A_OFF_BAR = A_OFF_ZONES + 1024;
     static constexpr int SMEM_AGG = A_OFF_BAR + 256 + 1024;
@@ -914,28 +919,30 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (g0 % n_c != 0) {
             const float *slot = prefix + static_cast<size_t>(blockIdx.x - 1) * CF::SLOT;
             if (warp_has_rows) {
+                // two feature blocks of loads in flight per step; element (c, r) at c * SROWS + r,
+                // so a warp reads consecutive floats
                 const bool mine = r <= LAST_ROW;
+                const float *col = slot + (mine ? r : 0);
 #pragma unroll 1
-                for (int f = 0; f < CF::NBLK; ++f) {
-                    uint32_t x[16];
+                for (int f = 0; f < CF::NBLK; f += 2) {
+                    uint32_t x[2][16];
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (mine)
-                            v4 = *reinterpret_cast<const float4 *>(slot + static_cast<size_t>(r) * CF::PP +
-                                                                   16 * f + j);
-                        x[j] = __float_as_uint(v4.x);
-                        x[j + 1] = __float_as_uint(v4.y);
-                        x[j + 2] = __float_as_uint(v4.z);
-                        x[j + 3] = __float_as_uint(v4.w);
-                    }
-                    tmem_st_x16(tmem + lo + CF::TM_S + 16 * f, x);
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int c = 16 * (f + h) + j;
+                            x[h][j] = (mine && c < CF::PP)
+                                          ? __float_as_uint(__ldg(col + static_cast<size_t>(c) * CF::SROWS))
+                                          : 0u;
+                        }
+                    tmem_st_x16(tmem + lo + CF::TM_S + 16 * f, x[0]);
+                    if (f + 1 < CF::NBLK) tmem_st_x16(tmem + lo + CF::TM_S + 16 * (f + 1), x[1]);
                 }
             }
             if constexpr (!CF::ZROW) {
-                const float *zrow = slot + static_cast<size_t>(V) * CF::PP;
-                const float za = r < CF::PP ? zrow[r] : 0.0f;
-                const float zb = r + 32 < CF::PP ? zrow[r + 32] : 0.0f;
+                const float *zcol = slot + V;
+                const float za = r < CF::PP ? zcol[static_cast<size_t>(r) * CF::SROWS] : 0.0f;
+                const float zb = r + 32 < CF::PP ? zcol[static_cast<size_t>(r + 32) * CF::SROWS] : 0.0f;
                 tmem_st_x1(tmem + lo + CF::TM_Z, __float_as_uint(za));
                 tmem_st_x1(tmem + lo + CF::TM_Z + 16, __float_as_uint(zb));
             }
@@ -969,10 +976,13 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle | warps 4-7: f(k) tiles |
 // warps 8-11: writer
 // ------------------------------------------------------------------------------------------------
-enum AggBar {
-    AB_TMA_FULL0 = 0, AB_STAGE_FREE0 = AB_TMA_FULL0 + kAggStages,
-    AB_PHIK_FULL0 = AB_STAGE_FREE0 + kAggStages, AB_PHIK_FREE0 = AB_PHIK_FULL0 + 2,
-    AB_AGG_DONE = AB_PHIK_FREE0 + 2, AB_COUNT
+// Barriers of the aggregate kernel with S k/v stages: TMA_FULL[S], STAGE_FREE[S], PHIK_FULL[2],
+// PHIK_FREE[2], AGG_DONE.
+template <int S>
+struct AggBar {
+    static constexpr int TMA_FULL0 = 0, STAGE_FREE0 = S, PHIK_FULL0 = 2 * S, PHIK_FREE0 = 2 * S + 2,
+                         AGG_DONE = 2 * S + 4, COUNT = 2 * S + 5;
+    static_assert(8 * COUNT + 8 <= 256, "barrier area");
 };
 
 template <int K, int V>
@@ -980,7 +990,11 @@ __global__ void __launch_bounds__(kAggThreads, 1)
 based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  float *__restrict__ slots, int H, int n_c, long long N, int G) {
     using CF = Cfg<K, V>;
-    constexpr int S = kAggStages;
+    constexpr int S = CF::A_NST;
+    using AB = AggBar<S>;
+    constexpr int AB_TMA_FULL0 = AB::TMA_FULL0, AB_STAGE_FREE0 = AB::STAGE_FREE0,
+                  AB_PHIK_FULL0 = AB::PHIK_FULL0, AB_PHIK_FREE0 = AB::PHIK_FREE0,
+                  AB_AGG_DONE = AB::AGG_DONE, AB_COUNT = AB::COUNT;
     if (!has_aggregate(N, G, blockIdx.x, n_c)) return;
     const Part part = cta_range(N, G, blockIdx.x);
     const long long ga = part.g0 > ((part.g1 - 1) / n_c) * n_c ? part.g0 : ((part.g1 - 1) / n_c) * n_c;
@@ -988,6 +1002,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int nchunks = static_cast<int>(g1 - ga);
 
     extern __shared__ uint8_t smem_raw[];
+    BASED_TRACE_INIT;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(smem);
@@ -1036,6 +1051,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                                         SITE_STAGE_FREE))
                     break;
                 const uint32_t bar = BAR(AB_TMA_FULL0 + s);
+                BASED_TRACE_EV(n + 40, 0);
                 mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
                 tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
                 tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
@@ -1061,6 +1077,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 const int s = n % S, pb = n & 1;
                 if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
                 if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (n >> 1) & 1, abort_flag, SITE_PHIK_FULL)) break;
+                BASED_TRACE_EV(n + 40, 1);
                 tc_fence_after();
                 const uint32_t lbo_a = CF::ZROW ? (CF::A_OFF_ONES - (CF::A_OFF_V + s * CF::VT)) : 16384u;
                 const uint64_t d_va = smem_desc(sb + CF::A_OFF_V + s * CF::VT, lbo_a, 1024, LAYOUT_SW128);
@@ -1077,6 +1094,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
                 mma_commit(BAR(AB_PHIK_FREE0 + pb));
                 mma_commit(BAR(AB_STAGE_FREE0 + s));
+                BASED_TRACE_EV(n + 40, 2);
             }
             mma_commit(BAR(AB_AGG_DONE));
             wait_bar(BAR(AB_AGG_DONE), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
@@ -1092,11 +1110,13 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (n >= 2 && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((n >> 1) - 1) & 1, abort_flag,
                                     SITE_PHIK_FREE))
                 break;
+            if (warp == 4 && lane == 0) BASED_TRACE_EV(n + 40, 3);
             build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
                               kBf16One2, kBf16One2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
+            if (warp == 4 && lane == 0) BASED_TRACE_EV(n + 40, 4);
         }
     } else {
         // writer: S^T rows (and z) -> fp32 slot
@@ -1107,19 +1127,24 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         float *slot = slots + static_cast<size_t>(blockIdx.x) * CF::SLOT;
         if (wait_bar(BAR(AB_AGG_DONE), 0, abort_flag, SITE_AGG_DONE)) {
             tc_fence_after();
+            if (warp == 8 && lane == 0) BASED_TRACE_EV(40, 5);
             if (q4 * 32 <= LAST_ROW) {
+                // two feature blocks per TMEM round trip; element (c, r) at c * SROWS + r
 #pragma unroll 1
-                for (int f = 0; f < CF::NBLK; ++f) {
-                    uint32_t x[16];
-                    tmem_ld_x16(tmem + lo + 16 * f, x);
-                    tmem_wait_ld();
+                for (int f = 0; f < CF::NBLK; f += 2) {
+                    uint32_t x[2][16];
+                    tmem_ld_x16(tmem + lo + 16 * f, x[0]);
+                    if (f + 1 < CF::NBLK) tmem_ld_x16(tmem + lo + 16 * (f + 1), x[1]);
+                    tmem_wait_ld_dep(x[0]);
+                    tmem_wait_ld_dep(x[1]);
                     if (r <= LAST_ROW) {
-                        float *dst = slot + static_cast<size_t>(r) * CF::PP + 16 * f;
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(dst + j) =
-                                make_float4(__uint_as_float(x[j]), __uint_as_float(x[j + 1]),
-                                            __uint_as_float(x[j + 2]), __uint_as_float(x[j + 3]));
+                        for (int h = 0; h < 2; ++h) {
+                            if (f + h >= CF::NBLK) break;
+                            float *dst = slot + static_cast<size_t>(16 * (f + h)) * CF::SROWS + r;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) dst[j * CF::SROWS] = __uint_as_float(x[h][j]);
+                        }
                     }
                 }
             }
@@ -1128,13 +1153,15 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 tmem_ld_x1(tmem + lo + CF::TA_Z, za);
                 tmem_ld_x1(tmem + lo + CF::TA_Z + 16, zb);
                 tmem_wait_ld();
-                float *zrow = slot + static_cast<size_t>(V) * CF::PP;
-                if (r < CF::PP && r < 128) zrow[r] = __uint_as_float(za);
-                if (r + 32 >= 128 && r + 32 < CF::PP) zrow[r + 32] = __uint_as_float(zb);
+                float *zcol = slot + V;  // element (c, V) at c * SROWS + V
+                if (r < CF::PP && r < 128) zcol[static_cast<size_t>(r) * CF::SROWS] = __uint_as_float(za);
+                if (r + 32 >= 128 && r + 32 < CF::PP)
+                    zcol[static_cast<size_t>(r + 32) * CF::SROWS] = __uint_as_float(zb);
             }
         }
     }
 
+    if (warp == 8 && lane == 0) BASED_TRACE_EV(40, 6);
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
