@@ -158,6 +158,24 @@ int check_args(const void *q, const void *k, const void *v, int B, int T, int H,
     return BASED_OK;
 }
 
+// Launches kernel<<<grid, block, smem, st>>>(args...), as a programmatic dependent of the
+// previous kernel in the stream when `dependent` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, bool dependent, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <int K, int V>
 int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
            float scale, float *o, float *ws, const Plan &p, DeviceState &d, cudaStream_t st,
@@ -187,14 +205,19 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
         BASED_CUDA(cudaGetLastError());
         if (p.runs.n > 0) {
             dim3 grid((p.slot_floats / 4 + 255) / 256, p.runs.n);
-            based_scan_kernel<<<grid, 256, 0, st>>>(ws, p.slot_floats, p.runs);
-            BASED_CUDA(cudaGetLastError());
+            BASED_CUDA(launch_dependent(based_scan_kernel, grid, dim3(256), 0, st, true, ws,
+                                        p.slot_floats, p.runs));
         }
     }
     if (ev_begin) BASED_CUDA(cudaEventRecord(ev_begin, st));
-    based_fwd_kernel<K, V><<<p.G, kFwdThreads, CF::SMEM_FWD, st>>>(mq, mk, mv, mo, ws, T, H, p.n_c,
-                                                                      p.N, p.G, scale);
-    BASED_CUDA(cudaGetLastError());
+    // A forward kernel that follows the aggregate pass is launched as its programmatic dependent
+    // (it starts while that pass finishes; only its read of the prefix slots waits). Without the
+    // aggregate pass, or when the caller brackets it with events, it is an ordinary launch: it
+    // must not start before earlier work in the stream that may produce q, k or v.
+    const bool dependent = p.need_agg && !ev_begin;
+    BASED_CUDA(launch_dependent(based_fwd_kernel<K, V>, dim3(p.G), dim3(kFwdThreads), CF::SMEM_FWD, st,
+                                dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
+                                p.N, p.G, scale));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }

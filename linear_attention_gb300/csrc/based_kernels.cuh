@@ -917,6 +917,9 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // A range that starts inside a head continues from the prefix state of the chunks before
         // it: load it into TMEM, then convert it like any other state.
         if (g0 % n_c != 0) {
+            // launched as a dependent of the aggregate / scan kernel: only this read of their
+            // output waits for them (every other role starts right away)
+            griddep_wait();
             const float *slot = prefix + static_cast<size_t>(blockIdx.x - 1) * CF::SLOT;
             if (warp_has_rows) {
                 // two feature blocks of loads in flight per step; element (c, r) at c * SROWS + r,
@@ -992,6 +995,9 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     using CF = Cfg<K, V>;
     constexpr int S = CF::A_NST;
     using AB = AggBar<S>;
+    // the scan / forward kernel may start launching now; it waits for this grid before it
+    // reads the slots
+    griddep_launch_dependents();
     constexpr int AB_TMA_FULL0 = AB::TMA_FULL0, AB_STAGE_FREE0 = AB::STAGE_FREE0,
                   AB_PHIK_FULL0 = AB::PHIK_FULL0, AB_PHIK_FREE0 = AB::PHIK_FREE0,
                   AB_AGG_DONE = AB::AGG_DONE, AB_COUNT = AB::COUNT;
@@ -1203,6 +1209,8 @@ inline ScanRuns make_scan_runs(long long N, int G, int n_c) {
 
 __global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems,
                                   const __grid_constant__ ScanRuns runs) {
+    griddep_launch_dependents();
+    griddep_wait();  // the aggregate kernel's slots are complete and visible
     const int r = blockIdx.y;
     if (r >= runs.n) return;
     const int i0 = runs.start[r], len = runs.len[r];
