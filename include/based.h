@@ -116,12 +116,15 @@ BASED_API int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint
                                 int H, int K, int V, float scale, float *o, based_stream_t stream);
 
 /*
- * based_fwd_host: the same computation on HOST buffers, end to end. Copies q, k, v to
- * library-owned device buffers (one cudaMemcpyAsync each), runs based_fwd on `stream`, copies o
- * back into the host buffer and synchronises `stream` before returning. Page-locked host memory
- * makes the copies asynchronous DMA; pageable memory also works, more slowly. The device buffers
- * are cached per device and grown on demand (cudaMalloc), so this call is not reentrant for one
- * device.
+ * based_fwd_host: the same computation on HOST buffers, end to end. The problem is cut into up to
+ * four pieces of independent heads (along B, or along H when B = 1); each piece is copied to
+ * library-owned device buffers, computed and copied back on one of three library-owned streams,
+ * so that the copies in both directions overlap each other and the kernels. The streams start
+ * after the work already queued on `stream`, which then continues after all of them; the call
+ * synchronises `stream` before returning. Page-locked host memory makes the copies asynchronous
+ * DMA; pageable memory also works, more slowly. The device buffers, the streams and one
+ * workspace per stream are cached per device and grown on demand (cudaMalloc), so this call is
+ * not reentrant for one device.
  */
 BASED_API int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_t *v_host, int B,
                    int T, int H, int K, int V, float scale, float *o_host, based_stream_t stream);

@@ -160,11 +160,21 @@ def test_caller_workspace_matches_library_workspace(cuda_device):
         based_fwd(q, k, v, workspace=ws[: nbytes // 2])
 
 
-def test_host_entry_point_matches_device_entry_point(cuda_device):
-    q, k, v = make_inputs(1, 1100, 4, 8, 128, 33)
+@pytest.mark.parametrize("shape", [(1, 1100, 4, 8, 128, 33), (3, 700, 2, 16, 64, 35),
+                                   (5, 300, 3, 16, 128, 36), (1, 520, 1, 8, 64, 37)])
+def test_host_entry_point_matches_device_entry_point(cuda_device, shape):
+    # The host entry point pipelines pieces of independent heads (along B, or along H for B = 1)
+    # through copies and kernels; the pieces' work partition may differ from the whole problem's,
+    # so the state sums may round differently: compare within a tight tolerance, and against the
+    # oracle's bar.
+    B, T, H, K, V, seed = shape
+    q, k, v = make_inputs(B, T, H, K, V, seed)
     o_dev = _run_gpu(q, k, v, None, cuda_device)
     o_host = based_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), device=cuda_device)
-    assert np.array_equal(o_dev, o_host.numpy())
+    assert np.allclose(o_host.numpy(), o_dev, rtol=1e-4, atol=1e-5)
+    ref, _ = oracle.chunked(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                            oracle.default_scale(K), chunk=128)
+    _assert_close(o_host.numpy(), ref, f"host entry {shape}")
 
 
 def test_output_not_written_past_end(cuda_device):
