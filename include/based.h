@@ -117,14 +117,13 @@ BASED_API int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint
 
 /*
  * based_fwd_host: the same computation on HOST buffers, end to end. The problem is cut into up to
- * four pieces of independent heads (along B, or along H when B = 1); each piece is copied to
- * library-owned device buffers, computed and copied back on one of three library-owned streams,
- * so that the copies in both directions overlap each other and the kernels. The streams start
- * after the work already queued on `stream`, which then continues after all of them; the call
- * synchronises `stream` before returning. Page-locked host memory makes the copies asynchronous
- * DMA; pageable memory also works, more slowly. The device buffers, the streams and one
- * workspace per stream are cached per device and grown on demand (cudaMalloc), so this call is
- * not reentrant for one device.
+ * eight pieces of independent heads (ranges of batch entries, or of heads when B = 1) that run through
+ * a three-stage pipeline on library-owned streams: copy in (pitched cudaMemcpy2DAsync), compute,
+ * copy out, so that both copy directions and the kernels overlap. The pipeline starts after the
+ * work already queued on `stream`, which then continues after it; the call synchronises `stream`
+ * before returning. Page-locked host memory makes the copies asynchronous DMA; pageable memory
+ * also works, more slowly. The device buffers, streams, events and workspace are cached per
+ * device and grown on demand (cudaMalloc), so this call is not reentrant for one device.
  */
 BASED_API int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_t *v_host, int B,
                    int T, int H, int K, int V, float scale, float *o_host, based_stream_t stream);

@@ -100,13 +100,14 @@ struct DeviceState {
     size_t ws_bytes = 0;
     void *hbuf = nullptr;  // based_fwd_host staging (q | k | v | o)
     size_t hbuf_bytes = 0;
-    // based_fwd_host pipeline: internal streams, their join events, one workspace per stream
-    static constexpr int kHostStreams = 3;
-    cudaStream_t hstream[kHostStreams] = {};
-    cudaEvent_t hjoin[kHostStreams] = {};
-    cudaEvent_t hfork = nullptr;
+    // based_fwd_host pipeline: copy-in, compute and copy-out streams, per-piece events, and the
+    // compute stream's workspace
+    static constexpr int kHostPieces = 8;
+    cudaStream_t hs_in = nullptr, hs_comp = nullptr, hs_out = nullptr;
+    cudaEvent_t hfork = nullptr, hdone = nullptr;
+    cudaEvent_t hin[kHostPieces] = {}, hcomp[kHostPieces] = {};
     void *hws = nullptr;
-    size_t hws_bytes = 0;  // per stream
+    size_t hws_bytes = 0;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -349,20 +350,20 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
     int dev, rc;
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
     DeviceState &d = g_dev[dev];
-    // The problem is cut into pieces of independent heads, along B (contiguous rows) or, for a
-    // single batch entry, along H (pitched copies); piece i runs on internal stream i % 3 as
-    // copy in -> forward pass -> copy out, so that the copies of neighbouring pieces overlap
-    // each other (both copy directions) and the kernels.
-    constexpr int kMaxPieces = 4;
-    const bool by_b = B >= 2;
-    const int parts = by_b ? (B < kMaxPieces ? B : kMaxPieces) : (H < kMaxPieces ? H : kMaxPieces);
+    // The problem is cut into up to 8 pieces of independent heads: ranges of batch entries (each
+    // a contiguous block) or, for a single batch entry, ranges of heads (pitched blocks of rows). A three-stage pipeline runs them: one
+    // stream copies every piece in, one computes each piece once its copy has landed, one copies
+    // each result out once it is computed, so that both copy directions and the kernels overlap.
+    constexpr int P = DeviceState::kHostPieces;
+    // whole batch entries where there are several (contiguous copies); head ranges otherwise
+    const int nb = B < P ? B : P;
+    const int nh = B > 1 ? 1 : (H < P ? H : P);
     const size_t rows = static_cast<size_t>(B) * T * H;
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     const size_t bq = up(rows * K * 2), bv = up(rows * V * 2), bo = up(rows * V * 4);
     const size_t need = 2 * bq + bv + bo;
-    // workspace of the largest piece
-    const int pb = by_b ? (B + parts - 1) / parts : B, ph = by_b ? H : (H + parts - 1) / parts;
-    const size_t ws_piece = up(make_plan(pb, T, ph, K, V, d.sms).ws_bytes);
+    // workspace of the largest piece (pieces run one after another on the compute stream)
+    const size_t ws_piece = up(make_plan((B + nb - 1) / nb, T, (H + nh - 1) / nh, K, V, d.sms).ws_bytes);
     uint8_t *base, *wsb;
     {
         std::lock_guard<std::mutex> lk(d.m);
@@ -383,15 +384,19 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
                 d.hws_bytes = 0;
                 if (e != cudaSuccess) return cuda_fail(e, "cudaFree(host-path workspace)");
             }
-            BASED_CUDA(cudaMalloc(&d.hws, ws_piece * DeviceState::kHostStreams));
+            BASED_CUDA(cudaMalloc(&d.hws, ws_piece));
             d.hws_bytes = ws_piece;
         }
         if (!d.hfork) {
-            BASED_CUDA(cudaEventCreateWithFlags(&d.hfork, cudaEventDisableTiming));
-            for (int i = 0; i < DeviceState::kHostStreams; ++i) {
-                BASED_CUDA(cudaStreamCreateWithFlags(&d.hstream[i], cudaStreamNonBlocking));
-                BASED_CUDA(cudaEventCreateWithFlags(&d.hjoin[i], cudaEventDisableTiming));
+            BASED_CUDA(cudaStreamCreateWithFlags(&d.hs_in, cudaStreamNonBlocking));
+            BASED_CUDA(cudaStreamCreateWithFlags(&d.hs_comp, cudaStreamNonBlocking));
+            BASED_CUDA(cudaStreamCreateWithFlags(&d.hs_out, cudaStreamNonBlocking));
+            BASED_CUDA(cudaEventCreateWithFlags(&d.hdone, cudaEventDisableTiming));
+            for (int i = 0; i < P; ++i) {
+                BASED_CUDA(cudaEventCreateWithFlags(&d.hin[i], cudaEventDisableTiming));
+                BASED_CUDA(cudaEventCreateWithFlags(&d.hcomp[i], cudaEventDisableTiming));
             }
+            BASED_CUDA(cudaEventCreateWithFlags(&d.hfork, cudaEventDisableTiming));
         }
         base = static_cast<uint8_t *>(d.hbuf);
         wsb = static_cast<uint8_t *>(d.hws);
@@ -401,51 +406,43 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
     uint16_t *dv = reinterpret_cast<uint16_t *>(base + 2 * bq);
     float *dout = reinterpret_cast<float *>(base + 2 * bq + bv);
     cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
-    // fork: the internal streams start after the work already queued on the caller's stream
+    // fork: the pipeline starts after the work already queued on the caller's stream
     BASED_CUDA(cudaEventRecord(d.hfork, caller));
-    const int nst = parts < DeviceState::kHostStreams ? parts : DeviceState::kHostStreams;
-    for (int i = 0; i < nst; ++i) BASED_CUDA(cudaStreamWaitEvent(d.hstream[i], d.hfork, 0));
-    const size_t rowb = static_cast<size_t>(T) * H;  // rows of one batch entry
-    for (int i = 0; i < parts; ++i) {
-        cudaStream_t st = d.hstream[i % nst];
-        void *ws = wsb + static_cast<size_t>(i % nst) * ws_piece;
-        if (by_b) {
-            const int b0 = static_cast<int>(static_cast<long long>(B) * i / parts);
-            const int b1 = static_cast<int>(static_cast<long long>(B) * (i + 1) / parts);
-            const size_t r0 = static_cast<size_t>(b0) * rowb, nr = static_cast<size_t>(b1 - b0) * rowb;
-            BASED_CUDA(cudaMemcpyAsync(dq + r0 * K, q_host + r0 * K, nr * K * 2, cudaMemcpyHostToDevice, st));
-            BASED_CUDA(cudaMemcpyAsync(dk + r0 * K, k_host + r0 * K, nr * K * 2, cudaMemcpyHostToDevice, st));
-            BASED_CUDA(cudaMemcpyAsync(dv + r0 * V, v_host + r0 * V, nr * V * 2, cudaMemcpyHostToDevice, st));
-            rc = run(dq + r0 * K, dk + r0 * K, dv + r0 * V, b1 - b0, T, H, K, V, scale, dout + r0 * V, ws,
-                     ws_piece, false, reinterpret_cast<based_stream_t>(st));
-            if (rc != BASED_OK) return rc;
-            BASED_CUDA(cudaMemcpyAsync(o_host + r0 * V, dout + r0 * V, nr * V * 4, cudaMemcpyDeviceToHost, st));
-        } else {
-            // heads [h0, h1) of the single batch entry: a compact (1, T, h1 - h0, .) problem
-            const int h0 = static_cast<int>(static_cast<long long>(H) * i / parts);
-            const int h1 = static_cast<int>(static_cast<long long>(H) * (i + 1) / parts);
-            const int hp = h1 - h0;
-            const size_t off = static_cast<size_t>(T) * h0;  // compact piece offset in rows
-            uint16_t *pq = dq + off * K, *pk = dk + off * K, *pv = dv + off * V;
-            float *po = dout + off * V;
-            BASED_CUDA(cudaMemcpy2DAsync(pq, hp * K * 2, q_host + h0 * K, H * K * 2, hp * K * 2, T,
-                                         cudaMemcpyHostToDevice, st));
-            BASED_CUDA(cudaMemcpy2DAsync(pk, hp * K * 2, k_host + h0 * K, H * K * 2, hp * K * 2, T,
-                                         cudaMemcpyHostToDevice, st));
-            BASED_CUDA(cudaMemcpy2DAsync(pv, hp * V * 2, v_host + h0 * V, H * V * 2, hp * V * 2, T,
-                                         cudaMemcpyHostToDevice, st));
-            rc = run(pq, pk, pv, 1, T, hp, K, V, scale, po, ws, ws_piece, false,
-                     reinterpret_cast<based_stream_t>(st));
-            if (rc != BASED_OK) return rc;
-            BASED_CUDA(cudaMemcpy2DAsync(o_host + h0 * V, H * V * 4, po, hp * V * 4, hp * V * 4, T,
-                                         cudaMemcpyDeviceToHost, st));
-        }
+    BASED_CUDA(cudaStreamWaitEvent(d.hs_in, d.hfork, 0));
+    BASED_CUDA(cudaStreamWaitEvent(d.hs_comp, d.hfork, 0));
+    BASED_CUDA(cudaStreamWaitEvent(d.hs_out, d.hfork, 0));
+    size_t off = 0;  // rows of the compact pieces before this one
+    for (int i = 0; i < nb * nh; ++i) {
+        const int ib = i / nh, ih = i % nh;
+        const int b0 = static_cast<int>(static_cast<long long>(B) * ib / nb);
+        const int b1 = static_cast<int>(static_cast<long long>(B) * (ib + 1) / nb);
+        const int h0 = static_cast<int>(static_cast<long long>(H) * ih / nh);
+        const int h1 = static_cast<int>(static_cast<long long>(H) * (ih + 1) / nh);
+        const int pb = b1 - b0, hp = h1 - h0;
+        const size_t prow = static_cast<size_t>(pb) * T;  // (b, t) rows of the piece
+        const size_t src = (static_cast<size_t>(b0) * T * H + h0);  // first element row on the host
+        uint16_t *pq = dq + off * K, *pk = dk + off * K, *pv = dv + off * V;
+        float *po = dout + off * V;
+        off += prow * hp;
+        BASED_CUDA(cudaMemcpy2DAsync(pq, hp * K * 2, q_host + src * K, H * K * 2, hp * K * 2, prow,
+                                     cudaMemcpyHostToDevice, d.hs_in));
+        BASED_CUDA(cudaMemcpy2DAsync(pk, hp * K * 2, k_host + src * K, H * K * 2, hp * K * 2, prow,
+                                     cudaMemcpyHostToDevice, d.hs_in));
+        BASED_CUDA(cudaMemcpy2DAsync(pv, hp * V * 2, v_host + src * V, H * V * 2, hp * V * 2, prow,
+                                     cudaMemcpyHostToDevice, d.hs_in));
+        BASED_CUDA(cudaEventRecord(d.hin[i], d.hs_in));
+        BASED_CUDA(cudaStreamWaitEvent(d.hs_comp, d.hin[i], 0));
+        rc = run(pq, pk, pv, pb, T, hp, K, V, scale, po, wsb, ws_piece, false,
+                 reinterpret_cast<based_stream_t>(d.hs_comp));
+        if (rc != BASED_OK) return rc;
+        BASED_CUDA(cudaEventRecord(d.hcomp[i], d.hs_comp));
+        BASED_CUDA(cudaStreamWaitEvent(d.hs_out, d.hcomp[i], 0));
+        BASED_CUDA(cudaMemcpy2DAsync(o_host + src * V, H * V * 4, po, hp * V * 4, hp * V * 4, prow,
+                                     cudaMemcpyDeviceToHost, d.hs_out));
     }
-    // join: the caller's stream continues after every piece, then the call waits for it
-    for (int i = 0; i < nst; ++i) {
-        BASED_CUDA(cudaEventRecord(d.hjoin[i], d.hstream[i]));
-        BASED_CUDA(cudaStreamWaitEvent(caller, d.hjoin[i], 0));
-    }
+    // join: the caller's stream continues after the last copy out, then the call waits for it
+    BASED_CUDA(cudaEventRecord(d.hdone, d.hs_out));
+    BASED_CUDA(cudaStreamWaitEvent(caller, d.hdone, 0));
     BASED_CUDA(cudaStreamSynchronize(caller));
     return BASED_OK;
 }
