@@ -91,9 +91,16 @@ __device__ __forceinline__ bool wait_bar_inline(uint32_t bar, uint32_t parity,
 }
 // The same wait as an out-of-line call: every role shares one copy of the loop, which keeps the
 // kernel's code (and its instruction-cache footprint) small.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                      uint32_t site, uint64_t limit_ns = kWaitLimitNs) {
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           uint32_t site, uint64_t limit_ns) {
     return wait_bar_inline(bar, parity, abort_flag, site, limit_ns);
+}
+// Bounded wait with the completed-phase test inline (a few instructions at each call site) and the
+// waiting loop out of line: a wait that finds its phase complete costs no call.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         uint32_t site, uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, site, limit_ns);
 }
 
 // ------------------------------------------------------------------------------------------------
