@@ -177,18 +177,21 @@ struct Cfg {
     static_assert(ZROW || OFF_PHIK + 8 * 4096 <= OFF_BAR, "z MMA window leaves shared memory");
     static_assert(SMEM_FWD <= 232448, "shared memory budget");
 
-    // Shared memory (aggregate kernel): two phi(k) buffers and as many k/v stages as fit (at
+    // Shared memory (aggregate kernel): A_NPHIK phi(k) buffers and as many k/v stages as fit (at
     // most 8), so that the loads run far enough ahead to hide the memory latency.
-    static constexpr int A_NST_FIT = (232448 - 1024 - 256 - 1024 - 2048 - align_up(2 * PHI, 1024)) / (RAW + VT);
+    // three f(k) buffers where they leave room for 4+ stages (the builders then run two chunks
+    // ahead of the state update), else two
+    static constexpr int A_NPHIK = (232448 - 4352 - align_up(3 * PHI, 1024)) / (RAW + VT) >= 4 ? 3 : 2;
+    static constexpr int A_NST_FIT = (232448 - 1024 - 256 - 1024 - 2048 - align_up(A_NPHIK * PHI, 1024)) / (RAW + VT);
     static constexpr int A_NST = A_NST_FIT < 8 ? A_NST_FIT : 8;
     static constexpr int A_OFF_PHIK = 0;
-    static constexpr int A_OFF_RAWK = align_up(2 * PHI, 1024);
+    static constexpr int A_OFF_RAWK = align_up(A_NPHIK * PHI, 1024);
     static constexpr int A_OFF_V = A_OFF_RAWK + A_NST * RAW;
     static constexpr int A_OFF_ONES = A_OFF_V + A_NST * VT;
     static constexpr int A_OFF_ZONES = align_up(A_OFF_ONES + ONES, 1024);
     static constexpr int A_OFF_BAR = A_OFF_ZONES + 1024;
     static constexpr int SMEM_AGG = A_OFF_BAR + 256 + 1024;
-    static_assert(ZROW || A_OFF_PHIK + PHI + 8 * 4096 <= A_OFF_BAR, "z MMA window (aggregate)");
+    static_assert(ZROW || A_OFF_PHIK + (A_NPHIK - 1) * PHI + 8 * 4096 <= A_OFF_BAR, "z MMA window (aggregate)");
     static_assert(SMEM_AGG <= 232448, "shared memory budget (aggregate)");
 };
 
@@ -249,11 +252,12 @@ __device__ __forceinline__ uint32_t taylor2(uint32_t s_lo, uint32_t s_hi, uint64
 // by half2 (bf16 pairs): (1, 1) and (1, 1) give f(k); (sigma, sigma) and (1/2, 1/2) give the
 // query side f~(q) = f(sigma q) with halved squares, so that f~(q).f(k) = 1 + sigma q.k +
 // sigma^2 (q.k)^2 / 2. (Multiplying by 1.0 is exact, so both sides share this one code path.)
+// Only blocks f_lo <= f < f_hi are built (two threads can share a token row).
 // Out of line: the q and k builders share one copy of the code, which keeps the kernel's
 // instruction-cache footprint small.
 template <int K>
 __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t sig2,
-                                            uint32_t half2) {
+                                            uint32_t half2, int f_lo, int f_hi) {
     const uint32_t rb = raw + static_cast<uint32_t>(t) * 32u;
     const uint32_t sw = static_cast<uint32_t>(((t >> 2) & 1) << 4);
     const uint4 lo = ld_shared_v4(rb + sw);
@@ -265,15 +269,18 @@ __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, u
     };
     constexpr uint32_t ONE_ZERO = 0x00003F80u;  // bf16 pair (1.0, 0.0)
     auto sq = [&](uint32_t x) { return bmul2(bmul2(x, half2), x); };
+    auto in = [&](int f) { return f_lo <= f && f < f_hi; };
     if constexpr (K == 16) {
         const uint4 hi = ld_shared_v4(rb + (16u ^ sw));
         uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
         for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], sig2);
-        store_blk(0, X[0], X[1], X[2], X[3], X[4], X[5], X[6], X[7]);
-        store_blk(1, sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]), sq(X[4]), sq(X[5]), sq(X[6]), sq(X[7]));
+        if (in(0)) store_blk(0, X[0], X[1], X[2], X[3], X[4], X[5], X[6], X[7]);
+        if (in(1))
+            store_blk(1, sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]), sq(X[4]), sq(X[5]), sq(X[6]), sq(X[7]));
 #pragma unroll
         for (int d = 1; d <= 7; ++d) {
+            if (!in(1 + d)) continue;
             uint32_t P[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
@@ -287,23 +294,26 @@ __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, u
             }
             store_blk(1 + d, P[0], P[1], P[2], P[3], P[4], P[5], P[6], P[7]);
         }
-        store_blk(9, bmul2(X[0], X[4]), bmul2(X[1], X[5]), bmul2(X[2], X[6]), bmul2(X[3], X[7]),
-                  ONE_ZERO, 0u, 0u, 0u);
+        if (in(9))
+            store_blk(9, bmul2(X[0], X[4]), bmul2(X[1], X[5]), bmul2(X[2], X[6]), bmul2(X[3], X[7]),
+                      ONE_ZERO, 0u, 0u, 0u);
     } else {
         uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
 #pragma unroll
         for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], sig2);
-        store_blk(0, X[0], X[1], X[2], X[3], sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]));
+        if (in(0)) store_blk(0, X[0], X[1], X[2], X[3], sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]));
         uint32_t R1[4], R3[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             R1[m] = __byte_perm(X[m], X[(m + 1) & 3], 0x5432);
             R3[m] = __byte_perm(X[(m + 1) & 3], X[(m + 2) & 3], 0x5432);
         }
-        store_blk(1, bmul2(X[0], R1[0]), bmul2(X[1], R1[1]), bmul2(X[2], R1[2]), bmul2(X[3], R1[3]),
-                  bmul2(X[0], X[1]), bmul2(X[1], X[2]), bmul2(X[2], X[3]), bmul2(X[3], X[0]));
-        store_blk(2, bmul2(X[0], R3[0]), bmul2(X[1], R3[1]), bmul2(X[2], R3[2]), bmul2(X[3], R3[3]),
-                  bmul2(X[0], X[2]), bmul2(X[1], X[3]), ONE_ZERO, 0u);
+        if (in(1))
+            store_blk(1, bmul2(X[0], R1[0]), bmul2(X[1], R1[1]), bmul2(X[2], R1[2]), bmul2(X[3], R1[3]),
+                      bmul2(X[0], X[1]), bmul2(X[1], X[2]), bmul2(X[2], X[3]), bmul2(X[3], X[0]));
+        if (in(2))
+            store_blk(2, bmul2(X[0], R3[0]), bmul2(X[1], R3[1]), bmul2(X[2], R3[2]), bmul2(X[3], R3[3]),
+                      bmul2(X[0], X[2]), bmul2(X[1], X[3]), ONE_ZERO, 0u);
     }
 }
 constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
@@ -776,7 +786,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !wait_bar(BAR(FB_PHIQ_FREE), (ro_idx - 1) & 1, abort_flag, SITE_PHIQ_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_BEGIN);
-            build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, sig2, kBf16Half2);
+            build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, sig2, kBf16Half2, 0,
+                              CF::NBLK);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIQ_FULL));
@@ -789,7 +800,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !wait_bar(BAR(FB_PHIK_FREE), (upd_idx - 1) & 1, abort_flag, SITE_PHIK_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIK_BEGIN);
-            build_features<K>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, kBf16One2, kBf16One2);
+            build_features<K>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, kBf16One2, kBf16One2, 0,
+                              CF::NBLK);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIK_FULL));
@@ -983,15 +995,15 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // ------------------------------------------------------------------------------------------------
 // Aggregate kernel: the partial state [S^T | z] of the last stretch of a range that ends inside a
 // head, written as fp32 rows into slot blockIdx.x.
-// warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle | warps 4-7: f(k) tiles |
-// warps 8-11: writer
+// warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle | warps 4-11: f(k) tiles (half of
+// each token row per warp), then warps 8-11 write the slot
 // ------------------------------------------------------------------------------------------------
-// Barriers of the aggregate kernel with S k/v stages: TMA_FULL[S], STAGE_FREE[S], PHIK_FULL[2],
-// PHIK_FREE[2], AGG_DONE.
-template <int S>
+// Barriers of the aggregate kernel with S k/v stages and NP f(k) buffers: TMA_FULL[S],
+// STAGE_FREE[S], PHIK_FULL[NP], PHIK_FREE[NP], AGG_DONE.
+template <int S, int NP>
 struct AggBar {
-    static constexpr int TMA_FULL0 = 0, STAGE_FREE0 = S, PHIK_FULL0 = 2 * S, PHIK_FREE0 = 2 * S + 2,
-                         AGG_DONE = 2 * S + 4, COUNT = 2 * S + 5;
+    static constexpr int TMA_FULL0 = 0, STAGE_FREE0 = S, PHIK_FULL0 = 2 * S, PHIK_FREE0 = 2 * S + NP,
+                         AGG_DONE = 2 * S + 2 * NP, COUNT = 2 * S + 2 * NP + 1;
     static_assert(8 * COUNT + 8 <= 256, "barrier area");
 };
 
@@ -1001,7 +1013,8 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                  float *__restrict__ slots, int H, int n_c, long long N, int G) {
     using CF = Cfg<K, V>;
     constexpr int S = CF::A_NST;
-    using AB = AggBar<S>;
+    constexpr int NP = CF::A_NPHIK;
+    using AB = AggBar<S, NP>;
     // the scan / forward kernel may start launching now; it waits for this grid before it
     // reads the slots
     griddep_launch_dependents();
@@ -1026,7 +1039,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < AB_COUNT; ++i)
-            mbar_init(BAR(i), (i == AB_PHIK_FULL0 || i == AB_PHIK_FULL0 + 1) ? 4u : 1u);
+            mbar_init(BAR(i), (i >= AB_PHIK_FULL0 && i < AB_PHIK_FULL0 + NP) ? 8u : 1u);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1087,9 +1100,9 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const uint32_t t_s = tmem, t_z = tmem + CF::TA_Z;
             const uint64_t d_zones = smem_desc(sb + CF::A_OFF_ZONES, 16, 256, LAYOUT_SW32);
             for (int n = 0; n < nchunks; ++n) {
-                const int s = n % S, pb = n & 1;
+                const int s = n % S, pb = n % NP;
                 if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
-                if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (n >> 1) & 1, abort_flag, SITE_PHIK_FULL)) break;
+                if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (n / NP) & 1, abort_flag, SITE_PHIK_FULL)) break;
                 BASED_TRACE_EV(n + 40, 1);
                 tc_fence_after();
                 const uint32_t lbo_a = CF::ZROW ? (CF::A_OFF_ONES - (CF::A_OFF_V + s * CF::VT)) : 16384u;
@@ -1114,25 +1127,28 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
     } else if (warp < 4) {
         // warps 2 and 3: no role (warp 2 owns the TMEM allocation)
-    } else if (warp < 8) {
-        // feature builders: token t of the chunk, alternating between two f(k) buffers
-        const int t = (warp - 4) * 32 + lane;
+    } else {
+        // feature builders (warps 4-11): token t of the chunk, warps 4-7 the first half of its
+        // feature blocks and warps 8-11 the second half, cycling through the f(k) buffers
+        const int t = (warp & 3) * 32 + lane;
+        const int f_lo = warp < 8 ? 0 : (CF::NBLK + 1) / 2, f_hi = warp < 8 ? (CF::NBLK + 1) / 2 : CF::NBLK;
         for (int n = 0; n < nchunks; ++n) {
-            const int s = n % S, pb = n & 1;
+            const int s = n % S, pb = n % NP;
             if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
-            if (n >= 2 && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((n >> 1) - 1) & 1, abort_flag,
-                                    SITE_PHIK_FREE))
+            if (n >= NP && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((n / NP) - 1) & 1, abort_flag,
+                                     SITE_PHIK_FREE))
                 break;
             if (warp == 4 && lane == 0) BASED_TRACE_EV(n + 40, 3);
             build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
-                              kBf16One2, kBf16One2);
+                              kBf16One2, kBf16One2, f_lo, f_hi);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
             if (warp == 4 && lane == 0) BASED_TRACE_EV(n + 40, 4);
         }
-    } else {
-        // writer: S^T rows (and z) -> fp32 slot
+    }
+    if (warp >= 8) {
+        // writer (warps 8-11, after building): S^T rows (and z) -> fp32 slot
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
