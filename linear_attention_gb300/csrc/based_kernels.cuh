@@ -407,6 +407,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int nchunks = static_cast<int>(g1 - g0);
     if (nchunks <= 0) return;
     BASED_TRACE_INIT;
+    if (threadIdx.x == 0) BASED_TRACE_EV(63, 20);  // CTA start
+#ifdef BASED_TRACE
+    if (threadIdx.x == 0 && trace_buf_ != nullptr)
+        trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 22] = global_timer_ns();
+#endif
 
     // ---- set-up: barriers, constant tiles, TMEM -------------------------------------------------
     if (threadIdx.x == 0) {
@@ -444,6 +449,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    if (threadIdx.x == 0) BASED_TRACE_EV(63, 21);  // set-up done
 
     if (warp == 0) {
         // ================================ TMA producer =========================================
@@ -990,6 +996,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+#ifdef BASED_TRACE
+    if (threadIdx.x == 0 && trace_buf_ != nullptr)
+        trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 23] = global_timer_ns();
+#endif
 }
 
 // ------------------------------------------------------------------------------------------------
