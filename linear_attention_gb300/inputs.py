@@ -41,6 +41,16 @@ WORKLOADS = {
     "ragged": Workload("ragged", 8, 3000, 12, 8, 128, 4, 0.3),
 }
 
+# The shape regime the "based_forward.py" spec grades in (its grader_shapes list; regime_md:
+# B 4-8, T 8192-16384, H 16-32, K in {8, 16}, V in {64, 128}), with the same input recipe.
+GRADER_WORKLOADS = {
+    "grader1": Workload("grader1", 4, 16384, 32, 16, 128, 101, None),
+    "grader2": Workload("grader2", 8, 8192, 32, 16, 128, 102, None),
+    "grader3": Workload("grader3", 8, 16384, 16, 16, 128, 103, None),
+    "grader4": Workload("grader4", 8, 16384, 32, 16, 64, 104, None),
+    "grader5": Workload("grader5", 8, 16384, 32, 8, 128, 105, None),
+}
+
 
 def make_inputs(B: int, T: int, H: int, K: int, V: int, seed: int, device="cpu"):
     """q, k, v ~ N(0,1) in bfloat16, drawn in the order q, k, v from one seeded CPU generator."""

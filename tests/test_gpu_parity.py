@@ -14,7 +14,7 @@ import torch
 import oracle
 from linear_attention_gb300.based import (BasedError, based_fwd, based_fwd_host, device_status,
                                           selftest_wait_timeout, workspace_size)
-from linear_attention_gb300.inputs import WORKLOADS, make_inputs, make_workload
+from linear_attention_gb300.inputs import GRADER_WORKLOADS, WORKLOADS, make_inputs, make_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -108,6 +108,20 @@ def test_workload_matches_oracle(name, cuda_device):
         got = np.stack([o[h // w.H, :, h % w.H, :] for h in heads])
         _assert_close(got, ref, (name, heads))
     assert np.isfinite(o).all()
+
+
+@pytest.mark.parametrize("name", list(GRADER_WORKLOADS))
+def test_grader_regime_matches_oracle(name, cuda_device):
+    """The spec's grading shapes (up to B=8, T=16384, H=32): two sampled heads, every row, against
+    the chunked oracle, plus finiteness of the whole output."""
+    w = GRADER_WORKLOADS[name]
+    q, k, v = make_workload(w)
+    o = _run_gpu(q, k, v, w.scale, cuda_device)
+    assert np.isfinite(o).all()
+    heads = [1, w.B * w.H - 2]
+    ref, _ = oracle.chunked(q, k, v, _scale(w.K, w.scale), chunk=256, heads=heads)
+    got = np.stack([o[h // w.H, :, h % w.H, :] for h in heads])
+    _assert_close(got, ref, (name, heads))
 
 
 def test_long_context_sampled_rows_direct_definition(cuda_device):
