@@ -413,6 +413,20 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 22] = global_timer_ns();
 #endif
 
+    // q, k, v tiles of chunk n (cursor position cu) into stage n % NST, completing on TMA_FULL
+    auto issue_loads = [&](int n, const Cursor &cu) {
+        const int s = n % CF::NST;
+        const uint32_t bar = BAR(FB_TMA_FULL0 + s);
+        BASED_TRACE_EV(n, TE_TMA_ISSUE);
+        mbar_arrive_expect_tx(bar, 2 * CF::RAW + CF::VT);
+        tma_load_4d(sb + CF::OFF_RAWQ + s * CF::RAW, &tm_q, bar, 0, cu.h, cu.t0(), cu.b);
+        tma_load_4d(sb + CF::OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
+        tma_load_4d(sb + CF::OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
+        if constexpr (V == 128)
+            tma_load_4d(sb + CF::OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(), cu.b);
+    };
+    const int n_early = nchunks < CF::NST ? nchunks : CF::NST;  // loads issued during set-up
+
     // ---- set-up: barriers, constant tiles, TMEM -------------------------------------------------
     if (threadIdx.x == 0) {
         // arrivals per phase: 1 = producer / commit, 4 = one elected lane per warp of a group
@@ -421,6 +435,15 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int i = 0; i < FB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
+        // the first loads go out now (this thread is the TMA producer), so that their memory
+        // latency overlaps the rest of the set-up
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_o);
+        Cursor cu;
+        cu.init(g0, nchunks, n_c, H);
+        for (int n = 0; n < n_early; ++n, cu.next()) issue_loads(n, cu);
     }
     // bf16 state operands: zero once (rows V+2.. stay zero; rows 0..V+1 are rewritten per use).
     for (int i = threadIdx.x; i < CF::NSBF * CF::SBF / 16; i += kFwdThreads)
@@ -454,27 +477,16 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 0) {
         // ================================ TMA producer =========================================
         if (lane == 0) {
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            prefetch_tensormap(&tm_o);
-            int issued = 0;
+            int issued = n_early;
             Cursor cu;
             cu.init(g0, nchunks, n_c, H);
-            for (int n = 0; n < nchunks; ++n, cu.next()) {
+            for (int n = 0; n < n_early; ++n) cu.next();
+            for (int n = n_early; n < nchunks; ++n, cu.next()) {
                 const int s = n % CF::NST;
-                if (n >= CF::NST && !wait_bar(BAR(FB_STAGE_FREE0 + s), ((n / CF::NST) - 1) & 1,
-                                              abort_flag, SITE_STAGE_FREE))
+                if (!wait_bar(BAR(FB_STAGE_FREE0 + s), ((n / CF::NST) - 1) & 1, abort_flag,
+                              SITE_STAGE_FREE))
                     break;
-                const uint32_t bar = BAR(FB_TMA_FULL0 + s);
-                BASED_TRACE_EV(n, TE_TMA_ISSUE);
-                mbar_arrive_expect_tx(bar, 2 * CF::RAW + CF::VT);
-                tma_load_4d(sb + CF::OFF_RAWQ + s * CF::RAW, &tm_q, bar, 0, cu.h, cu.t0(), cu.b);
-                tma_load_4d(sb + CF::OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
-                tma_load_4d(sb + CF::OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
-                if constexpr (V == 128)
-                    tma_load_4d(sb + CF::OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(),
-                                cu.b);
+                issue_loads(n, cu);
                 ++issued;
             }
             if (*abort_flag) {  // let copies already in flight land before the CTA exits
@@ -1047,11 +1059,29 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::A_OFF_BAR + 8 * AB_COUNT + 4);
     auto BAR = [&](int i) -> uint32_t { return sb + CF::A_OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
+    // k, v tiles of stretch chunk n (cursor position cu) into stage n % S, completing on TMA_FULL
+    auto issue_loads = [&](int n, const Cursor &cu) {
+        const int s = n % S;
+        const uint32_t bar = BAR(AB_TMA_FULL0 + s);
+        BASED_TRACE_EV(n + 40, 0);
+        mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
+        tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
+        tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
+        if constexpr (V == 128)
+            tma_load_4d(sb + CF::A_OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(), cu.b);
+    };
+    const int n_early = nchunks < S ? nchunks : S;  // loads issued during set-up
     if (threadIdx.x == 0) {
         for (int i = 0; i < AB_COUNT; ++i)
             mbar_init(BAR(i), (i >= AB_PHIK_FULL0 && i < AB_PHIK_FULL0 + NP) ? 8u : 1u);
         *abort_flag = 0;
         fence_mbar_init();
+        // the first loads go out now (this thread is the TMA producer)
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        Cursor cu;
+        cu.init(ga, nchunks, n_c, H);
+        for (int n = 0; n < n_early; ++n, cu.next()) issue_loads(n, cu);
     }
     if constexpr (CF::ZROW) {
         for (int i = threadIdx.x; i < CF::ONES / 16; i += kAggThreads)
@@ -1076,24 +1106,15 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     if (warp == 0) {
         if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            int issued = 0;
+            int issued = n_early;
             Cursor cu;
             cu.init(ga, nchunks, n_c, H);
-            for (int n = 0; n < nchunks; ++n, cu.next()) {
+            for (int n = 0; n < n_early; ++n) cu.next();
+            for (int n = n_early; n < nchunks; ++n, cu.next()) {
                 const int s = n % S;
-                if (n >= S && !wait_bar(BAR(AB_STAGE_FREE0 + s), ((n / S) - 1) & 1, abort_flag,
-                                        SITE_STAGE_FREE))
+                if (!wait_bar(BAR(AB_STAGE_FREE0 + s), ((n / S) - 1) & 1, abort_flag, SITE_STAGE_FREE))
                     break;
-                const uint32_t bar = BAR(AB_TMA_FULL0 + s);
-                BASED_TRACE_EV(n + 40, 0);
-                mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
-                tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
-                tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
-                if constexpr (V == 128)
-                    tma_load_4d(sb + CF::A_OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(),
-                                cu.b);
+                issue_loads(n, cu);
                 ++issued;
             }
             if (*abort_flag) {
