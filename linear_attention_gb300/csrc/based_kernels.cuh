@@ -957,6 +957,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // launched as a dependent of the aggregate / scan kernel: only this read of their
             // output waits for them (every other role starts right away)
             griddep_wait();
+#ifdef BASED_TRACE
+            if (r == 0 && trace_buf_ != nullptr)
+                trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 24] = global_timer_ns();
+#endif
             const float *slot = prefix + static_cast<size_t>(blockIdx.x - 1) * CF::SLOT;
             if (warp_has_rows) {
                 // two feature blocks of loads in flight per step; element (c, r) at c * SROWS + r,
@@ -1051,6 +1055,10 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
     extern __shared__ uint8_t smem_raw[];
     BASED_TRACE_INIT;
+#ifdef BASED_TRACE
+    if (threadIdx.x == 0 && trace_buf_ != nullptr)
+        trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 40) * 32 + 8] = global_timer_ns();
+#endif
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(smem);
@@ -1222,6 +1230,10 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
 
     if (warp == 8 && lane == 0) BASED_TRACE_EV(40, 6);
+#ifdef BASED_TRACE
+    if (warp == 8 && lane == 0 && trace_buf_ != nullptr)
+        trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 40) * 32 + 9] = global_timer_ns();
+#endif
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
