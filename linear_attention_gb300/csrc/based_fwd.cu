@@ -87,6 +87,7 @@ struct Plan {
     int slot_floats;
     size_t ws_bytes;
     ScanRuns runs;  // runs of ranges whose partial states chain into one head's prefix
+    bool scan;      // some prefix chains more than kMaxChain partial states: run the scan kernel
 };
 
 constexpr int kMaxDevices = 64;
@@ -140,6 +141,9 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms) {
     for (int i = 0; i < p.G; ++i)
         if (has_aggregate(p.N, p.G, i, p.n_c)) p.need_agg = true;
     p.runs = make_scan_runs(p.N, p.G, p.n_c);
+    p.scan = false;
+    for (int r = 0; r < p.runs.n; ++r)
+        if (p.runs.len[r] > kMaxChain) p.scan = true;
     p.slot_floats = slot_floats(K, V);
     p.ws_bytes = p.need_agg ? static_cast<size_t>(p.G) * p.slot_floats * sizeof(float) : 0;
     return p;
@@ -211,7 +215,7 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     if (p.need_agg) {
         based_agg_kernel<K, V><<<p.G, kAggThreads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.N, p.G);
         BASED_CUDA(cudaGetLastError());
-        if (p.runs.n > 0) {
+        if (p.scan) {  // otherwise each forward CTA sums the (at most kMaxChain) states it needs
             dim3 grid((p.slot_floats / 4 + 255) / 256, p.runs.n);
             BASED_CUDA(launch_dependent(based_scan_kernel, grid, dim3(256), 0, st, true, ws,
                                         p.slot_floats, p.runs));
@@ -225,7 +229,7 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     const bool dependent = p.need_agg && !ev_begin;
     BASED_CUDA(launch_dependent(based_fwd_kernel<K, V>, dim3(p.G), dim3(kFwdThreads), CF::SMEM_FWD, st,
                                 dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
-                                p.N, p.G, scale));
+                                p.N, p.G, scale, p.scan ? 1 : kMaxChain));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }
@@ -324,7 +328,7 @@ int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
     int dev;
     if (current_device(&dev) != BASED_OK) return 0;
     const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms);
-    return p.need_agg ? (p.runs.n > 0 ? 3 : 2) : 1;
+    return p.need_agg ? (p.scan ? 3 : 2) : 1;
 }
 
 size_t based_fwd_workspace_size(int B, int T, int H, int K, int V) {

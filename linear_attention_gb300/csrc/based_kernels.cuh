@@ -17,12 +17,14 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <type_traits>
 
 #include "sm103_ptx.cuh"
 
 namespace based {
 
 constexpr int kChunk = 128;            // rows per chunk = MMA M
+constexpr int kMaxChain = 2;           // partial states a forward CTA sums into its prefix itself
 constexpr int kFwdThreads = 512;       // 4 warpgroups
 constexpr int kAggThreads = 384;       // 3 warpgroups
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after 1 s
@@ -340,6 +342,14 @@ __host__ __device__ __forceinline__ bool continues_prefix(long long N, int G, in
     const Part p = cta_range(N, G, i);
     return p.g1 > p.g0 && (p.g0 % n_c) != 0 && (p.g0 / n_c) == ((p.g1 - 1) / n_c);
 }
+// Partial states that make up the prefix of range i (which starts inside a head): slots
+// i - m .. i - 1, where the ranges i - m + 1 .. i - 1 continue the prefix of the one before them.
+// m stops at max_chain (1 when a scan has already summed each run into its last slot).
+__host__ __device__ __forceinline__ int prefix_chain_len(long long N, int G, int i, int n_c, int max_chain) {
+    int m = 1;
+    for (int j = i - 1; m < max_chain && continues_prefix(N, G, j, n_c); --j) ++m;
+    return m;
+}
 
 // Walks the chunks of a range without divisions: (b, h, c) advance like an odometer.
 struct Cursor {
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G,
-                 float scale) {
+                 float scale, int max_chain) {
     using CF = Cfg<K, V>;
     constexpr bool FAST = CF::FAST;
     extern __shared__ uint8_t smem_raw[];
@@ -954,6 +964,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // A range that starts inside a head continues from the prefix state of the chunks before
         // it: load it into TMEM, then convert it like any other state.
         if (g0 % n_c != 0) {
+            // The prefix is the sum of the partial states of the ranges since the head's last
+            // range boundary that starts a stretch: slots blockIdx - m .. blockIdx - 1 (m <= max_chain;
+            // max_chain = 1 when a scan has already summed them into slot blockIdx - 1).
+            const int m = prefix_chain_len(N, G, static_cast<int>(blockIdx.x), n_c, max_chain);
             // launched as a dependent of the aggregate / scan kernel: only this read of their
             // output waits for them (every other role starts right away)
             griddep_wait();
@@ -961,35 +975,49 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (r == 0 && trace_buf_ != nullptr)
                 trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 24] = global_timer_ns();
 #endif
-            const float *slot = prefix + static_cast<size_t>(blockIdx.x - 1) * CF::SLOT;
-            if (warp_has_rows) {
-                // two feature blocks of loads in flight per step; element (c, r) at c * SROWS + r,
-                // so a warp reads consecutive floats
-                const bool mine = r <= LAST_ROW;
-                const float *col = slot + (mine ? r : 0);
+            const float *slot = prefix + static_cast<size_t>(blockIdx.x - m) * CF::SLOT;
+            // One code path per chain length, so that every load it issues is needed and all of a
+            // step's loads are in flight together; the terms are summed in range order.
+            auto load_prefix = [&](auto chain_len) {
+                constexpr int M = decltype(chain_len)::value;
+                auto chain = [&](const float *e) -> float {
+                    float x = __ldg(e);
+#pragma unroll
+                    for (int i = 1; i < M; ++i) x += __ldg(e + static_cast<size_t>(i) * CF::SLOT);
+                    return x;
+                };
+                if (warp_has_rows) {
+                    // two feature blocks of loads in flight per step; element (c, r) at
+                    // c * SROWS + r, so a warp reads consecutive floats
+                    const bool mine = r <= LAST_ROW;
+                    const float *col = slot + (mine ? r : 0);
 #pragma unroll 1
-                for (int f = 0; f < CF::NBLK; f += 2) {
-                    uint32_t x[2][16];
+                    for (int f = 0; f < CF::NBLK; f += 2) {
+                        uint32_t x[2][16];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                        for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int c = 16 * (f + h) + j;
-                            x[h][j] = (mine && c < CF::PP)
-                                          ? __float_as_uint(__ldg(col + static_cast<size_t>(c) * CF::SROWS))
-                                          : 0u;
-                        }
-                    tmem_st_x16(tmem + lo + CF::TM_S + 16 * f, x[0]);
-                    if (f + 1 < CF::NBLK) tmem_st_x16(tmem + lo + CF::TM_S + 16 * (f + 1), x[1]);
+                            for (int j = 0; j < 16; ++j) {
+                                const int c = 16 * (f + h) + j;
+                                x[h][j] = (mine && c < CF::PP)
+                                              ? __float_as_uint(chain(col + static_cast<size_t>(c) * CF::SROWS))
+                                              : 0u;
+                            }
+                        tmem_st_x16(tmem + lo + CF::TM_S + 16 * f, x[0]);
+                        if (f + 1 < CF::NBLK) tmem_st_x16(tmem + lo + CF::TM_S + 16 * (f + 1), x[1]);
+                    }
                 }
-            }
-            if constexpr (!CF::ZROW) {
-                const float *zcol = slot + V;
-                const float za = r < CF::PP ? zcol[static_cast<size_t>(r) * CF::SROWS] : 0.0f;
-                const float zb = r + 32 < CF::PP ? zcol[static_cast<size_t>(r + 32) * CF::SROWS] : 0.0f;
-                tmem_st_x1(tmem + lo + CF::TM_Z, __float_as_uint(za));
-                tmem_st_x1(tmem + lo + CF::TM_Z + 16, __float_as_uint(zb));
-            }
+                if constexpr (!CF::ZROW) {
+                    const float *zcol = slot + V;
+                    const float za = r < CF::PP ? chain(zcol + static_cast<size_t>(r) * CF::SROWS) : 0.0f;
+                    const float zb = r + 32 < CF::PP ? chain(zcol + static_cast<size_t>(r + 32) * CF::SROWS) : 0.0f;
+                    tmem_st_x1(tmem + lo + CF::TM_Z, __float_as_uint(za));
+                    tmem_st_x1(tmem + lo + CF::TM_Z + 16, __float_as_uint(zb));
+                }
+            };
+            static_assert(kMaxChain == 2, "one prefix load path per chain length");
+            if (m == 1) load_prefix(std::integral_constant<int, 1>{});
+            else load_prefix(std::integral_constant<int, 2>{});
             tmem_wait_st();
             convert(cidx++, 63);
         }

@@ -1,7 +1,8 @@
 // Host-only check of the work partition used by the Based kernels (compiled with nvcc, run on
 // the CPU): for many shapes and SM counts, every chunk is covered exactly once, each range that
-// starts inside a head finds in slot i-1 (after the scan) exactly the chunks of that head before
-// it, and no aggregate slot is read that the aggregate pass did not write.
+// starts inside a head finds exactly the chunks of that head before it, either in slot i-1 after
+// the scan or, when every run is at most kMaxChain long (no scan), in the slots it sums itself,
+// and no aggregate slot is read that the aggregate pass did not write.
 #include <cstdio>
 #include <vector>
 
@@ -32,8 +33,31 @@ int main() {
                 }
                 for (long long g = 0; g < N; ++g)
                     if (covered[g] != 1) { printf("chunk %lld covered %d times\n", g, covered[g]); return 1; }
-                // scan over the runs the host lists: slot j takes the chunks of slot j-1
+                // without a scan: the slots a prefixed range sums are adjacent stretches of its
+                // head that end at its first chunk and start at the head's first chunk
                 const ScanRuns runs = make_scan_runs(N, G, n_c);
+                bool scan = false;
+                for (int r = 0; r < runs.n; ++r) scan = scan || runs.len[r] > kMaxChain;
+                if (!scan) {
+                    for (int i = 0; i < G; ++i) {
+                        const Part p = cta_range(N, G, i);
+                        if (p.g0 % n_c == 0) continue;
+                        const long long h = p.g0 / n_c;
+                        const int m = prefix_chain_len(N, G, i, n_c, kMaxChain);
+                        if (m < 1 || m > kMaxChain || i - m < 0) { printf("bad chain length\n"); return 1; }
+                        long long end = p.g0;
+                        for (int j = i - 1; j >= i - m; --j) {
+                            if (hd[j] != h || hi[j] != end) { printf("chain gap: i=%d j=%d\n", i, j); return 1; }
+                            end = lo[j];
+                        }
+                        if (end != h * n_c) {
+                            printf("chain short: sms=%d heads=%d T=%d i=%d\n", sms, heads, T, i);
+                            return 1;
+                        }
+                        ++checked;
+                    }
+                }
+                // scan over the runs the host lists: slot j takes the chunks of slot j-1
                 for (int r = 0; r < runs.n; ++r) {
                     const int i0 = runs.start[r], len = runs.len[r];
                     if (len < 2 || i0 + len > G) { printf("bad run\n"); return 1; }

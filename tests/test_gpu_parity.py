@@ -70,6 +70,11 @@ SMALL = [
     (2, 700, 3, 8, 128, 21, 0.3),
     (1, 1536, 1, 16, 128, 22, None),
     (2, 4096, 8, 8, 64, 23, None),
+    # the forward kernel sums up to two partial states into a prefix itself (no scan kernel)
+    (1, 1100, 64, 16, 64, 24, None),
+    (3, 1500, 40, 8, 128, 25, 0.3),
+    (3, 1024, 24, 8, 64, 26, None),
+    (2, 1100, 32, 16, 128, 27, 0.4),
 ]
 
 
