@@ -41,9 +41,9 @@ def canonical_flops(B, T, H, K, V, C=64):
     return B * H * T * (4 * P * V + 2 * C * (K + V))
 
 
-def algorithmic_bytes(B, T, H, K, V):
-    """q, k, v read once (bf16) and o written once (fp32)."""
-    return B * T * H * (2 * K * 2 + V * 2 + V * 4)
+def algorithmic_bytes(B, T, H, K, V, out_bytes=4):
+    """q, k, v read once (bf16) and o written once (fp32, or bf16 with out_bytes=2)."""
+    return B * T * H * (2 * K * 2 + V * 2 + V * out_bytes)
 
 
 def load_peaks():
@@ -265,20 +265,34 @@ def run_reference(args, w, world, rank):
 def run_gpu(args, w, world, rank, local):
     from linear_attention_gb300 import build as lbuild
     lbuild.build()
-    from linear_attention_gb300.based import (based_fwd, based_fwd_host, based_fwd_timed,
-                                              device_status, kernel_count)
+    from linear_attention_gb300.based import (based_fwd, based_fwd_bf16_out, based_fwd_host,
+                                              based_fwd_timed, device_status, kernel_count)
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
     q0, k0, v0 = make_workload(w)
-    wbytes = algorithmic_bytes(B, T, H, K, V)
+    obf = args.out == "bf16"
+    out_dtype = torch.bfloat16 if obf else torch.float32
+    wbytes = algorithmic_bytes(B, T, H, K, V, 2 if obf else 4)
+
+    def fwd(s, stream=None):
+        if obf:
+            based_fwd_bf16_out(*s[:3], scale=w.scale, out=s[3], stream=stream)
+        else:
+            based_fwd(*s[:3], scale=w.scale, out=s[3], stream=stream)
+
+    def fwd_timed(s, eb, ee, stream):
+        if obf:
+            based_fwd_bf16_out(*s[:3], scale=w.scale, out=s[3], stream=stream, events=(eb, ee))
+        else:
+            based_fwd_timed(s[0], s[1], s[2], s[3], eb, ee, scale=w.scale, stream=stream)
     # rotate enough input/output sets that consecutive steps never find their data in L2
     nsets = max(2, -(-3 * L2_BYTES // wbytes) + 1)
     sets = []
     for i in range(nsets):
         sets.append((q0.to(dev), k0.to(dev), v0.to(dev),
-                     torch.empty(B, T, H, V, dtype=torch.float32, device=dev)))
+                     torch.empty(B, T, H, V, dtype=out_dtype, device=dev)))
     stream = torch.cuda.current_stream(dev)
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -290,15 +304,14 @@ def run_gpu(args, w, world, rank, local):
     # warm-up: W steps, then keep stepping for at least 1 s so clocks settle under load
     clocks = ClockSampler(local).start() if (rank == 0 and not args.profile) else None
     for i in range(max(3, args.warmup)):
-        based_fwd(*sets[i % nsets][:3], scale=w.scale, out=sets[i % nsets][3])
+        fwd(sets[i % nsets])
     torch.cuda.synchronize(dev)
     t_end = time.time() + (0.0 if args.profile else 1.0)
     i = 0
     while time.time() < t_end or (clocks is not None and clocks.nsamples() < 3 and
                                   time.time() < t_end + 5):
         for _ in range(20):
-            s = sets[i % nsets]
-            based_fwd(*s[:3], scale=w.scale, out=s[3])
+            fwd(sets[i % nsets])
             i += 1
         torch.cuda.synchronize(dev)
 
@@ -307,8 +320,7 @@ def run_gpu(args, w, world, rank, local):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for j in range(args.steps):
-        s = sets[j % nsets]
-        based_fwd(*s[:3], scale=w.scale, out=s[3], stream=stream)
+        fwd(sets[j % nsets], stream)
     t_stop.record(stream)
     torch.cuda.synchronize(dev)
     dist_barrier(world)
@@ -319,8 +331,7 @@ def run_gpu(args, w, world, rank, local):
     # not shortened by early start)
     torch.cuda.synchronize(dev)
     for j in range(args.steps):
-        s = sets[j % nsets]
-        based_fwd_timed(s[0], s[1], s[2], s[3], ev_b[j], ev_e[j], scale=w.scale, stream=stream)
+        fwd_timed(sets[j % nsets], ev_b[j], ev_e[j], stream)
     torch.cuda.synchronize(dev)
     fwd_ms = [ev_b[j].elapsed_time(ev_e[j]) for j in range(args.steps)]
     elapsed_ms = dist_max(elapsed_ms, world, dev)
@@ -342,7 +353,10 @@ def run_gpu(args, w, world, rank, local):
 
     # end-to-end through the host entry point: pinned host inputs -> GPU -> pinned host output
     e2e = None
-    if not args.profile:
+    if obf:
+        e2e = {"value": None, "unit": "tokens/s",
+               "note": "the host entry point (based_fwd_host) returns fp32 only"}
+    elif not args.profile:
         qh, kh, vh = q0.pin_memory(), k0.pin_memory(), v0.pin_memory()
         oh = torch.empty(B, T, H, V, dtype=torch.float32).pin_memory()
         for _ in range(3):
@@ -368,7 +382,10 @@ def run_gpu(args, w, world, rank, local):
         "data": "synthetic",
         "config": workload_config(w, {
             "l2": f"{nsets} rotating input/output sets ({nsets * wbytes / 2**20:.0f} MiB > 3x L2)",
-            "launch": "stream launches, one based_fwd call per step (aggregate, scan and forward kernels; the scan and forward kernels as programmatic dependents)"}),
+            "output": "bf16" if obf else "fp32",
+            "launch": f"stream launches, one {'based_fwd_bf16_out' if obf else 'based_fwd'} call per step "
+                      f"({launches} kernel(s): aggregate, scan when a prefix chains more than two "
+                      "partial states, forward; the later ones as programmatic dependents)"}),
         "tflops": flops / (ms_per_step * 1e-3) / 1e12,
         "pct_bf16_peak": 100.0 * flops / (ms_per_step * 1e-3) / (tc * 1e12),
         "pct_roofline_step": 100.0 * t_roof_ms / ms_per_step,
@@ -395,6 +412,8 @@ def main():
     ap.add_argument("--workload", default="headline", choices=sorted(WORKLOADS) + sorted(GRADER_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out", default="fp32", choices=["fp32", "bf16"],
+                    help="output dtype (fp32 is the contract's default; bf16 uses based_fwd_bf16_out)")
     ap.add_argument("--profile", action="store_true",
                     help="only the W warm-up and K timed steps (for running under ncu)")
     args = ap.parse_args()

@@ -91,6 +91,22 @@ BASED_API int based_fwd_ws(const uint16_t *q, const uint16_t *k, const uint16_t 
                  based_stream_t stream);
 
 /*
+ * based_fwd_bf16_out: based_fwd with a bfloat16 output, which halves the largest data stream of
+ * the call (the kernel-task spec's output contract allows "bf16 or fp32"; fp32 is the default).
+ *   q, k, v, B, T, H, K, V, scale, stream: as for based_fwd.
+ *   o          device, bf16 bit patterns, (B,T,H,V) contiguous, 16-byte aligned (written). Each
+ *              element is the fp32 result based_fwd computes, rounded to nearest even.
+ *   workspace  NULL: the library-owned workspace (as based_fwd); otherwise a caller-owned device
+ *              workspace of ws_bytes bytes (as based_fwd_ws).
+ *   ev_begin, ev_end  NULL, or caller-created CUDA events recorded around the forward kernel
+ *              (as based_fwd_timed).
+ * Errors: as based_fwd and based_fwd_ws; o must not overlap q, k or v.
+ */
+BASED_API int based_fwd_bf16_out(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T,
+                                 int H, int K, int V, float scale, uint16_t *o, void *workspace,
+                                 size_t ws_bytes, based_stream_t stream, void *ev_begin, void *ev_end);
+
+/*
  * based_fwd_noalloc: based_fwd for callers that may not allocate device memory while they run,
  * e.g. a serving loop whose device memory is planned up front by its own allocator, or code
  * that cannot afford the device-wide synchronisation cudaMalloc/cudaFree can cause. The paper

@@ -44,6 +44,10 @@ def _load():
                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_void_p]
     L.based_fwd_timed.restype = i
+    L.based_fwd_bf16_out.argtypes = [u16p, u16p, u16p, i, i, i, i, i, ctypes.c_float, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+    L.based_fwd_bf16_out.restype = i
     L.based_fwd_kernel_count.argtypes = [i, i, i, i, i]
     L.based_fwd_kernel_count.restype = i
     L.based_fwd_workspace_size.argtypes = [i, i, i, i, i]
@@ -122,6 +126,33 @@ def based_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional
                                 _scale_arg(scale), out.data_ptr(), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), st.cuda_stream)
     _check(rc, "based_fwd")
+    return out
+
+
+def based_fwd_bf16_out(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+                       out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       events: Optional[tuple] = None) -> torch.Tensor:
+    """based_fwd with a bf16 output: o (B,T,H,V) bf16, each element the fp32 result rounded to
+    nearest even. ``workspace`` as for based_fwd; ``events`` = (ev_begin, ev_end), already-recorded
+    torch CUDA events, brackets the forward kernel as in based_fwd_timed."""
+    L = _load()
+    B, T, H, K, V = _shapes(q, k, v)
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("based_fwd_bf16_out takes CUDA tensors")
+    if out is None:
+        out = torch.empty(B, T, H, V, dtype=torch.bfloat16, device=q.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (B, T, H, V) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 tensor of shape (B,T,H,V)")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (
+        workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    eb, ee = (None, None) if events is None else (events[0].cuda_event, events[1].cuda_event)
+    with torch.cuda.device(q.device):
+        st = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = L.based_fwd_bf16_out(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                                  _scale_arg(scale), out.data_ptr(), ws_ptr, ws_bytes,
+                                  st.cuda_stream, eb, ee)
+    _check(rc, "based_fwd_bf16_out")
     return out
 
 

@@ -96,7 +96,7 @@ struct DeviceState {
     bool init = false;
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
-    bool attrs_done[2][2] = {{false, false}, {false, false}};
+    bool attrs_done[2][2][2] = {};  // [K == 16][V == 128][bf16 output]
     void *ws = nullptr;
     size_t ws_bytes = 0;
     void *hbuf = nullptr;  // based_fwd_host staging (q | k | v | o)
@@ -149,8 +149,9 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms) {
     return p;
 }
 
+// out_elem: bytes per output element (4 for fp32, 2 for bf16)
 int check_args(const void *q, const void *k, const void *v, int B, int T, int H, int K, int V,
-               const void *o) {
+               const void *o, size_t out_elem = 4) {
     if (!q || !k || !v || !o) return BASED_ERR_NULL_POINTER;
     if (K != 8 && K != 16) return BASED_ERR_UNSUPPORTED_K;
     if (V != 64 && V != 128) return BASED_ERR_UNSUPPORTED_V;
@@ -163,7 +164,7 @@ int check_args(const void *q, const void *k, const void *v, int B, int T, int H,
         const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
         return x < y + nb && y < x + na;
     };
-    const size_t ob = rows * V * 4;
+    const size_t ob = rows * V * out_elem;
     if (overlap(o, ob, q, rows * K * 2) || overlap(o, ob, k, rows * K * 2) ||
         overlap(o, ob, v, rows * V * 2))
         return BASED_ERR_ALIASING;
@@ -188,16 +189,16 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-template <int K, int V>
+template <int K, int V, bool OBF>
 int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
-           float scale, float *o, float *ws, const Plan &p, DeviceState &d, cudaStream_t st,
+           float scale, void *o, float *ws, const Plan &p, DeviceState &d, cudaStream_t st,
            cudaEvent_t ev_begin, cudaEvent_t ev_end) {
     using CF = Cfg<K, V>;
     {
         std::lock_guard<std::mutex> lk(d.m);
-        bool &done = d.attrs_done[K == 16][V == 128];
+        bool &done = d.attrs_done[K == 16][V == 128][OBF];
         if (!done) {
-            BASED_CUDA(cudaFuncSetAttribute(based_fwd_kernel<K, V>,
+            BASED_CUDA(cudaFuncSetAttribute(based_fwd_kernel<K, V, OBF>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_FWD));
             BASED_CUDA(cudaFuncSetAttribute(based_agg_kernel<K, V>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_AGG));
@@ -210,7 +211,9 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != BASED_OK) return rc;
-    if ((rc = make_map(&mo, o, V, B, T, H, 32, CU_TENSOR_MAP_SWIZZLE_128B, true, CF::EPI_ROWS)) != BASED_OK)
+    // output boxes of 128-byte rows: 32 fp32 or 64 bf16 columns
+    if ((rc = make_map(&mo, o, V, B, T, H, OBF ? 64 : 32, CU_TENSOR_MAP_SWIZZLE_128B, !OBF, CF::EPI_ROWS)) !=
+        BASED_OK)
         return rc;
     if (p.need_agg) {
         based_agg_kernel<K, V><<<p.G, kAggThreads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.N, p.G);
@@ -227,17 +230,18 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     // aggregate pass, or when the caller brackets it with events, it is an ordinary launch: it
     // must not start before earlier work in the stream that may produce q, k or v.
     const bool dependent = p.need_agg && !ev_begin;
-    BASED_CUDA(launch_dependent(based_fwd_kernel<K, V>, dim3(p.G), dim3(kFwdThreads), CF::SMEM_FWD, st,
+    BASED_CUDA(launch_dependent(based_fwd_kernel<K, V, OBF>, dim3(p.G), dim3(kFwdThreads), CF::SMEM_FWD, st,
                                 dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
                                 p.N, p.G, scale, p.scan ? 1 : kMaxChain));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }
 
+// obf: o holds bf16 (else fp32)
 int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H, int K, int V,
-        float scale, float *o, void *ws, size_t ws_bytes, bool own_ws, based_stream_t stream,
+        float scale, void *o, bool obf, void *ws, size_t ws_bytes, bool own_ws, based_stream_t stream,
         void *ev_begin = nullptr, void *ev_end = nullptr) {
-    int rc = check_args(q, k, v, B, T, H, K, V, o);
+    int rc = check_args(q, k, v, B, T, H, K, V, o, obf ? 2 : 4);
     if (rc != BASED_OK) return rc;
     int dev;
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
@@ -265,10 +269,16 @@ int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, i
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float *w = static_cast<float *>(ws);
     cudaEvent_t eb = static_cast<cudaEvent_t>(ev_begin), ee = static_cast<cudaEvent_t>(ev_end);
-    if (K == 16 && V == 64) return launch<16, 64>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
-    if (K == 16 && V == 128) return launch<16, 128>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
-    if (K == 8 && V == 64) return launch<8, 64>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
-    return launch<8, 128>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    if (obf) {
+        if (K == 16 && V == 64) return launch<16, 64, true>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+        if (K == 16 && V == 128) return launch<16, 128, true>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+        if (K == 8 && V == 64) return launch<8, 64, true>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+        return launch<8, 128, true>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    }
+    if (K == 16 && V == 64) return launch<16, 64, false>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    if (K == 16 && V == 128) return launch<16, 128, false>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    if (K == 8 && V == 64) return launch<8, 64, false>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
+    return launch<8, 128, false>(q, k, v, B, T, H, scale, o, w, p, d, st, eb, ee);
 }
 
 // Scratch of based_fwd_noalloc: a fixed array in the library's device image, so that the entry
@@ -301,13 +311,13 @@ extern "C" {
 
 int based_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H, int K,
               int V, float scale, float *o, based_stream_t stream) {
-    return run(q, k, v, B, T, H, K, V, scale, o, nullptr, 0, true, stream);
+    return run(q, k, v, B, T, H, K, V, scale, o, false, nullptr, 0, true, stream);
 }
 
 int based_fwd_timed(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
                     int K, int V, float scale, float *o, based_stream_t stream, void *ev_begin,
                     void *ev_end) {
-    return run(q, k, v, B, T, H, K, V, scale, o, nullptr, 0, true, stream, ev_begin, ev_end);
+    return run(q, k, v, B, T, H, K, V, scale, o, false, nullptr, 0, true, stream, ev_begin, ev_end);
 }
 
 int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
@@ -320,7 +330,7 @@ int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
     if (p.ws_bytes > BASED_NOALLOC_SCRATCH_BYTES) return BASED_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     if (p.ws_bytes > 0 && (rc = noalloc_scratch(dev, &scratch)) != BASED_OK) return rc;
-    return run(q, k, v, B, T, H, K, V, scale, o, scratch, p.ws_bytes, false, stream);
+    return run(q, k, v, B, T, H, K, V, scale, o, false, scratch, p.ws_bytes, false, stream);
 }
 
 int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
@@ -341,7 +351,14 @@ size_t based_fwd_workspace_size(int B, int T, int H, int K, int V) {
 int based_fwd_ws(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
                  int K, int V, float scale, float *o, void *workspace, size_t ws_bytes,
                  based_stream_t stream) {
-    return run(q, k, v, B, T, H, K, V, scale, o, workspace, ws_bytes, false, stream);
+    return run(q, k, v, B, T, H, K, V, scale, o, false, workspace, ws_bytes, false, stream);
+}
+
+int based_fwd_bf16_out(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H,
+                       int K, int V, float scale, uint16_t *o, void *workspace, size_t ws_bytes,
+                       based_stream_t stream, void *ev_begin, void *ev_end) {
+    return run(q, k, v, B, T, H, K, V, scale, o, true, workspace, ws_bytes, workspace == nullptr,
+               stream, ev_begin, ev_end);
 }
 
 int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_t *v_host, int B,
@@ -436,7 +453,7 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
                                      cudaMemcpyHostToDevice, d.hs_in));
         BASED_CUDA(cudaEventRecord(d.hin[i], d.hs_in));
         BASED_CUDA(cudaStreamWaitEvent(d.hs_comp, d.hin[i], 0));
-        rc = run(pq, pk, pv, pb, T, hp, K, V, scale, po, wsb, ws_piece, false,
+        rc = run(pq, pk, pv, pb, T, hp, K, V, scale, po, false, wsb, ws_piece, false,
                  reinterpret_cast<based_stream_t>(d.hs_comp));
         if (rc != BASED_OK) return rc;
         BASED_CUDA(cudaEventRecord(d.hcomp[i], d.hs_comp));
@@ -513,7 +530,7 @@ const char *based_strerror(int code) {
 
 const char *based_last_cuda_error(void) { return tl_cuda_error; }
 
-int based_abi_version(void) { return 10000; }
+int based_abi_version(void) { return 10100; }
 
 #ifdef BASED_TRACE
 // Trace builds only: device buffer of (CTAs x 64 x 32) uint64 stage timestamps, or NULL to stop.

@@ -395,7 +395,9 @@ enum FwdBar {
     FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_DRAIN_B, FB_AV_DONE1, FB_COUNT
 };
 
-template <int K, int V>
+// OBF: the output tile is written as bf16 (round to nearest even from the fp32 quotient) instead
+// of fp32.
+template <int K, int V, bool OBF>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -736,11 +738,12 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         int ro_idx = 0, upd_idx = 0;
         bool ok = true;
 
-        // Output tile: o = O_num / (O_den + 1e-6), written through staging buffers as 32-column
-        // pieces (SW128) by TMA stores, so that the output traffic never occupies the load/store
-        // path the TMEM accesses of the other roles use. Either each warp stages and stores its
-        // own 32 rows (EPI_ROWS = 32: the four warps never wait for each other), or the four
-        // warps meet at a named barrier and one thread stores the 128-row piece (fewer stores).
+        // Output tile: o = O_num / (O_den + 1e-6), written through staging buffers as pieces of
+        // 128-byte rows (32 fp32 or 64 bf16 columns, SW128) by TMA stores, so that the output
+        // traffic never occupies the load/store path the TMEM accesses of the other roles use.
+        // Either each warp stages and stores its own 32 rows (EPI_ROWS = 32: the four warps never
+        // wait for each other), or the four warps meet at a named barrier and one thread stores
+        // the 128-row piece (fewer stores).
         // Rows past T are clipped by the tensor map; a box that starts past T is not issued.
         int piece = 0;  // output pieces staged so far (selects the staging buffer)
         auto epilogue = [&](int m, int eb, int eh, int et0) -> bool {
@@ -763,17 +766,17 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (warp == 11 && lane == 0) BASED_TRACE_EV(m, TE_EPI_OFREE);
             };
             if constexpr (V == 64) release_o();
+            constexpr int PCOLS = OBF ? 64 : 32;  // output columns per 128-byte staged row
 #pragma unroll
-            for (int p = 0; p < V / 32; ++p) {
+            for (int p = 0; p < V / PCOLS; ++p) {
                 if constexpr (V == 128) {
-                    if (p == 2) {
+                    if (p == 64 / PCOLS) {
                         tmem_ld_x32(to + 64, r0);
                         tmem_ld_x32(to + 96, r1);
                         tmem_wait_ld();
                         release_o();
                     }
                 }
-                const uint32_t *r = (p & 1) ? r1 : r0;
                 constexpr bool WARP_BOX = CF::EPI_ROWS == 32;
                 const uint32_t ost = sb + CF::OFF_OST + (piece % CF::NOST) * CF::OST + q4 * 4096;
                 ++piece;
@@ -785,23 +788,34 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (WARP_BOX) __syncwarp();
                 else named_bar_sync(1, 128);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(ost + static_cast<uint32_t>(lane) * 128u + ((c ^ (lane & 7)) << 4),
-                                 __float_as_uint(__uint_as_float(r[4 * c]) * inv),
-                                 __float_as_uint(__uint_as_float(r[4 * c + 1]) * inv),
-                                 __float_as_uint(__uint_as_float(r[4 * c + 2]) * inv),
-                                 __float_as_uint(__uint_as_float(r[4 * c + 3]) * inv));
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t a = ost + static_cast<uint32_t>(lane) * 128u + ((c ^ (lane & 7)) << 4);
+                    if constexpr (OBF) {
+                        // 16 bytes = 8 bf16 columns: columns 0..31 from r0, 32..63 from r1
+                        const uint32_t *x = (c < 4 ? r0 : r1) + 8 * (c & 3);
+                        auto o2 = [&](int j) {
+                            return pack_bf16x2(__uint_as_float(x[j]) * inv, __uint_as_float(x[j + 1]) * inv);
+                        };
+                        st_shared_v4(a, o2(0), o2(2), o2(4), o2(6));
+                    } else {
+                        const uint32_t *r = (p & 1) ? r1 : r0;
+                        st_shared_v4(a, __float_as_uint(__uint_as_float(r[4 * c]) * inv),
+                                     __float_as_uint(__uint_as_float(r[4 * c + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(r[4 * c + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(r[4 * c + 3]) * inv));
+                    }
+                }
                 fence_proxy_async_smem();
                 if (WARP_BOX) {
                     __syncwarp();
                     if (lane == 0 && et0 + 32 * q4 < T) {
-                        tma_store_4d(&tm_o, ost, 32 * p, eh, et0 + 32 * q4, eb);
+                        tma_store_4d(&tm_o, ost, PCOLS * p, eh, et0 + 32 * q4, eb);
                         bulk_commit_group();
                     }
                 } else {
                     named_bar_sync(1, 128);
                     if (t == 0) {
-                        tma_store_4d(&tm_o, ost - q4 * 4096, 32 * p, eh, et0, eb);
+                        tma_store_4d(&tm_o, ost - q4 * 4096, PCOLS * p, eh, et0, eb);
                         bulk_commit_group();
                     }
                 }

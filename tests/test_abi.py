@@ -48,7 +48,7 @@ def test_strerror_names_every_code(lib):
     for code in range(0, -12, -1):
         assert lib.based_strerror(code).decode() != "unknown error code"
     assert lib.based_strerror(-99).decode() == "unknown error code"
-    assert lib.based_abi_version() == 10000
+    assert lib.based_abi_version() == 10100
 
 
 def _call(lib, q=16, k=16, v=16, B=1, T=8, H=1, K=16, V=64, o=4096):
@@ -70,6 +70,23 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert _call(lib, **{**ok, "v": base + (2 << 20) + 8}) == -5
     assert _call(lib, **{**ok, "o": ok["v"] + 64}) == -6
     assert _call(lib, **{**ok, "o": ok["q"]}) == -6
+
+
+def test_bf16_output_argument_errors(lib):
+    # same checks on the bf16-output entry point; its output spans B*T*H*V*2 bytes
+    def call(q, k, v, o, B=1, T=8, H=1, K=16, V=64):
+        return lib.based_fwd_bf16_out(q, k, v, B, T, H, K, V, ctypes.c_float(-1.0), o, None, 0,
+                                      None, None, None)
+    base = 1 << 40
+    q, k, v = base, base + (1 << 20), base + (2 << 20)
+    assert call(q, k, v, 0) == -1
+    assert call(q, k, v, base + (3 << 20), K=12) == -2
+    assert call(q, k, v, base + (3 << 20), V=32) == -3
+    assert call(q, k, v, base + (3 << 20) + 2) == -5
+    assert call(q, k, v, v + 64) == -6
+    # a bf16 output of 8 rows x 64 spans 1024 bytes: one that starts 1008 bytes before q
+    # overlaps it
+    assert call(q, k, v, q - 1008) == -6
 
 
 def test_partition_and_prefix_slots():
