@@ -385,9 +385,10 @@ struct Cursor {
 
 // ------------------------------------------------------------------------------------------------
 // Forward kernel
-// warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle (warp 2 owns TMEM)
-// warps 4-7: Taylor weights A | warps 8-11: feature tiles + output epilogue | warps 12-15: state
-// conversion S^T (fp32 TMEM) -> bf16 operand
+// warp 0: TMA producer | warp 1: intra-chunk MMA issuer | warp 2: owns TMEM | warp 3: state MMA
+// issuer | warps 4-7: Taylor weights A | warps 8-11: feature tiles + output epilogue |
+// warps 12-15: state conversion S^T (fp32 TMEM) -> bf16 operand. V = 64: warps 2 and 15 compute
+// Taylor weights too (warp 15 has no rows of S^T to convert).
 // ------------------------------------------------------------------------------------------------
 enum FwdBar {
     FB_TMA_FULL0 = 0, FB_STAGE_FREE0 = 3, FB_S_FULL = 6, FB_A_FULL, FB_O_FULL0, FB_O_FULL1,
@@ -441,9 +442,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     // ---- set-up: barriers, constant tiles, TMEM -------------------------------------------------
     if (threadIdx.x == 0) {
-        // arrivals per phase: 1 = producer / commit, 4 = one elected lane per warp of a group
-        // STAGE_FREE: one commit from each MMA issuer
-        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, 4, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, 4, 4, 1, 1, 1};
+        // arrivals per phase: 1 = producer / commit, else one elected lane per warp of a group;
+        // STAGE_FREE: one commit from each MMA issuer. V = 64: six warps compute the Taylor
+        // weights and three convert the state (see the role split below).
+        constexpr uint32_t NW = FAST ? 6 : 4, NC = FAST ? 3 : 4;
+        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, NW, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, NC, NC, 1, 1, 1};
         for (int i = 0; i < FB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -532,18 +535,23 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             Cursor cu;
             cu.init(g0, nchunks, n_c, H);
             if (warp == 1) {
-                // ---- intra-chunk stream: QK(0); per chunk AV(n), QK(n + 1) ----
+                // ---- intra-chunk stream: QK(0); per chunk QK(n + 1) and AV(n) ----
                 constexpr uint32_t ID_QK = idesc_bf16_f32(128, 128, 0, 0);
                 constexpr uint32_t ID_AV = idesc_bf16_f32(128, FAST ? CF::NO : V, 0, 1);
                 constexpr uint32_t ID_RS = idesc_bf16_f32(128, 16, 0, 0);
                 const uint64_t d_q = smem_desc(sb + CF::OFF_RAWQ, 16, 256, LAYOUT_SW32);
                 const uint64_t d_k = smem_desc(sb + CF::OFF_RAWK, 16, 256, LAYOUT_SW32);
-                bool ok = wait_bar(BAR(FB_TMA_FULL0), 0, abort_flag, SITE_TMA_FULL);
-                if (ok) {
+                // s = q k^T of chunk m into the scores tile, completing on S_FULL
+                auto issue_qk = [&](int m) -> bool {
+                    const int sm = m % CF::NST;
+                    if (!wait_bar(BAR(FB_TMA_FULL0 + sm), (m / CF::NST) & 1, abort_flag, SITE_TMA_FULL))
+                        return false;
                     tc_fence_after();
-                    mma_ss(t_sc, d_q, d_k, ID_QK, 0);
+                    mma_ss(t_sc, dadd(d_q, sm * CF::RAW), dadd(d_k, sm * CF::RAW), ID_QK, 0);
                     mma_commit(BAR(FB_S_FULL));
-                }
+                    return true;
+                };
+                bool ok = issue_qk(0);
                 for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
                     const int s = n % CF::NST;
                     const int ob = FAST ? (n & 1) : 0;
@@ -551,6 +559,18 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const uint32_t t_out = ob ? t_o1 : t_o0;
                     if (!(ok = wait_bar(BAR(FB_A_FULL), n & 1, abort_flag, SITE_A_FULL))) break;
                     BASED_TRACE_EV(n, TE_A_READY);
+                    // V = 64: the scores tile is free once A(n) is complete, so QK(n + 1) goes
+                    // first when its tiles have landed, and the Taylor weights of chunk n + 1 are
+                    // computed while AV(n) runs (they wait for AV_DONE before they overwrite A).
+                    bool qk_next = false;
+                    if constexpr (FAST) {
+                        const int m = n + 1;
+                        if (m < nchunks && mbar_test_wait(BAR(FB_TMA_FULL0 + m % CF::NST), (m / CF::NST) & 1)) {
+                            if (!(ok = issue_qk(m))) break;
+                            qk_next = true;
+                            BASED_TRACE_EV(n, TE_QK_ISSUED);
+                        }
+                    }
                     if (FAST ? (n >= 2) : (n >= 1)) {
                         const uint32_t par = FAST ? (((n >> 1) - 1) & 1) : ((n - 1) & 1);
                         if (!(ok = wait_bar(BAR(FB_O_FREE0 + ob), par, abort_flag, SITE_O_FREE))) break;
@@ -572,18 +592,12 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!cu.has_ro()) mma_commit(BAR(FB_O_FULL0 + ob));  // no read-out follows
                     mma_commit(BAR(FB_STAGE_FREE0 + s));                  // QK(n) and AV(n) read it
                     BASED_TRACE_EV(n, TE_AV_ISSUED);
-                    if (n + 1 < nchunks) {
+                    if (n + 1 < nchunks && !qk_next) {
                         if constexpr (!FAST) {
                             // the next s overwrites A (same TMEM columns): wait until A was read
                             if (!(ok = wait_bar(BAR(FB_AV_DONE), n & 1, abort_flag, SITE_AV_DONE))) break;
                         }
-                        const int s1 = (n + 1) % CF::NST;
-                        if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s1), ((n + 1) / CF::NST) & 1, abort_flag,
-                                          SITE_TMA_FULL)))
-                            break;
-                        tc_fence_after();
-                        mma_ss(t_sc, dadd(d_q, s1 * CF::RAW), dadd(d_k, s1 * CF::RAW), ID_QK, 0);
-                        mma_commit(BAR(FB_S_FULL));
+                        if (!(ok = issue_qk(n + 1))) break;
                         BASED_TRACE_EV(n, TE_QK_ISSUED);
                     }
                 }
@@ -601,9 +615,13 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint64_t d_phiq = smem_desc(sb + CF::OFF_PHIQ, 16, 256, LAYOUT_SW32);
                 int ro_idx = 0, upd_idx = 0;
                 bool ok = true;
-                auto issue_ro = [&](int n, uint32_t t_out) -> bool {
+                // release_stage >= 0: that stage is released as soon as f~(q_c) is built (the
+                // builders have read its raw tiles; the commit tracks the state update issued
+                // before, which read v_c)
+                auto issue_ro = [&](int n, uint32_t t_out, int release_stage) -> bool {
                     // O += f~(q_c) [S | z_hi z_lo], after O = A [v_c | 1] has completed
                     if (!wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)) return false;
+                    if (release_stage >= 0) mma_commit(BAR(FB_STAGE_FREE0 + release_stage));
                     if (!wait_bar(BAR(FB_SBF_FULL), ro_idx & 1, abort_flag, SITE_SBF_FULL)) return false;
                     const int ob = FAST ? (n & 1) : 0;
                     const uint32_t avp = FAST ? ((n >> 1) & 1) : (n & 1);
@@ -652,22 +670,31 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     // first, so that the single state operand is consumed before it is rewritten
                     if (FAST && cu.has_upd() && !(ok = issue_upd(n, d_va))) break;
                     if (cu.has_ro()) {
-                        if (!(ok = issue_ro(n, t_out))) break;
+                        if (!(ok = issue_ro(n, t_out, FAST ? s : -1))) break;
                         mma_commit(BAR(FB_O_FULL0 + ob));
                         BASED_TRACE_EV(n, TE_RO_ISSUED);
                     }
                     if (!FAST && cu.has_upd() && !(ok = issue_upd(n, d_va))) break;
-                    mma_commit(BAR(FB_STAGE_FREE0 + s));  // UPD(n) read v_c; f(k), f~(q) are built
+                    // UPD(n) read v_c; f(k), f~(q) are built (V = 64 with a read-out: released above)
+                    if (!(FAST && cu.has_ro())) mma_commit(BAR(FB_STAGE_FREE0 + s));
                 }
                 mma_commit(BAR(FB_DRAIN_B));
                 wait_bar(BAR(FB_DRAIN_B), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
             }
         }
-    } else if (warp == 2) {
+    } else if (warp == 2 && !FAST) {
         // warp 2: no role besides owning the TMEM allocation
-    } else if (warp < 8) {
+    } else if (warp < 8 || (FAST && warp == 15)) {
         // ======================= Taylor weights: A = poly(s), causal mask =======================
+        // Query rows 32 q4 .. 32 q4 + 31 (TMEM lane quarter q4 = warp % 4) need key blocks
+        // 0..q4 of 32 keys. V = 64: warps 2 and 15, otherwise idle (warp 15 has no state rows to
+        // convert), share the two longest row quarters, so that no warp computes more than two
+        // blocks: warp 6 blocks 0-1 and warp 2 block 2 of quarter 2, warp 7 blocks 0-1 and
+        // warp 15 blocks 2-3 of quarter 3.
         const int q4 = warp & 3;
+        const bool helper = FAST && (warp == 2 || warp == 15);
+        const int kb_lo = helper ? 2 : 0;
+        const int kb_hi = (FAST && !helper && q4 >= 2) ? 1 : q4;
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
         const float c1 = scale, c2 = 0.5f * scale * scale;
         const uint64_t C1 = pack_f32x2(c1, c1), C2 = pack_f32x2(c2, c2), ONE = pack_f32x2(1.f, 1.f);
@@ -676,7 +703,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t z16[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) z16[j] = 0u;
-            for (int kb = q4 + 1; kb < 4; ++kb) tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, z16);
+            if (!helper)
+                for (int kb = q4 + 1; kb < 4; ++kb) tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, z16);
             tmem_wait_st();
         }
         // mask of the diagonal block, per bf16 pair (keys 2i, 2i+1 against row = lane)
@@ -687,39 +715,62 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!wait_bar(BAR(FB_S_FULL), n & 1, abort_flag, SITE_S_FULL)) break;
             tc_fence_after();
             if (warp == 7 && lane == 0) BASED_TRACE_EV(n, TE_POLY_BEGIN);
-            uint32_t z16[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) z16[j] = 0u;
-            // Key blocks 0..q4 of 32 keys (blocks above the diagonal block are zero), one per step
-            // with the load of the next one in flight. Rolled by two blocks (one copy of the body
-            // keeps the code small).
             uint32_t ra[32], rb[32];
-            tmem_ld_x32(tmem + lo + CF::TM_SC, ra);
-            auto weights = [&](int kb, uint32_t (&r)[32]) {
+            tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * kb_lo, ra);
+            // weights of key block kb from its 32 scores, as 16 bf16 pairs
+            auto pack_weights = [&](int kb, const uint32_t (&r)[32], uint32_t (&packed)[16]) {
                 const bool diag = kb == q4;
-                uint32_t packed[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     packed[i] = taylor2(r[2 * i], r[2 * i + 1], C2, C1, ONE) &
                                 (diag ? diag_mask(i) : 0xFFFFFFFFu);
-                // V = 128: A columns [16 kb, 16 kb + 16) overlay s columns already read
-                tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, packed);
             };
-#pragma unroll 1
-            for (int kb = 0; kb <= q4; kb += 2) {
-                const bool two = kb + 1 <= q4;
-                if (two) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb + 1), rb);
+            if constexpr (FAST) {
+                // At most two key blocks per warp, both loaded and weighted before A, which AV of
+                // the previous chunk may still be reading, is overwritten (QK of this chunk can be
+                // issued before that AV).
+                const bool two = kb_lo < kb_hi;
+                if (two) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb_lo + 1), rb);
                 tmem_wait_ld_dep(ra);
-                if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kb == 0 ? TE_POLY_LD0 : TE_POLY_LD1);
-                weights(kb, ra);
+                if (warp == 7 && lane == 0) BASED_TRACE_EV(n, TE_POLY_LD0);
+                uint32_t pa[16], pb[16];
+                pack_weights(kb_lo, ra, pa);
                 if (two) {
-                    if (kb + 2 <= q4) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb + 2), ra);
                     tmem_wait_ld_dep(rb);
-                    weights(kb + 1, rb);
+                    pack_weights(kb_lo + 1, rb, pb);
                 }
-            }
-            if constexpr (!FAST) {
-                // V = 128: A overlays s, so the blocks above the diagonal block are cleared each time
+                if (n > 0 && !wait_bar(BAR(((n - 1) & 1) ? FB_AV_DONE1 : FB_AV_DONE), ((n - 1) >> 1) & 1,
+                                       abort_flag, SITE_AV_DONE))
+                    break;
+                tc_fence_after();
+                tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb_lo, pa);
+                if (two) tmem_st_x16(tmem + lo + CF::TM_A + 16 * (kb_lo + 1), pb);
+            } else {
+                // Key blocks 0..q4, one per step with the load of the next one in flight. Rolled
+                // by two blocks (one copy of the body keeps the code small). A columns
+                // [16 kb, 16 kb + 16) overlay s columns already read.
+                auto weights = [&](int kb, const uint32_t (&r)[32]) {
+                    uint32_t packed[16];
+                    pack_weights(kb, r, packed);
+                    tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, packed);
+                };
+#pragma unroll 1
+                for (int kb = kb_lo; kb <= kb_hi; kb += 2) {
+                    const bool two = kb + 1 <= kb_hi;
+                    if (two) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb + 1), rb);
+                    tmem_wait_ld_dep(ra);
+                    if (warp == 7 && lane == 0) BASED_TRACE_EV(n, kb == 0 ? TE_POLY_LD0 : TE_POLY_LD1);
+                    weights(kb, ra);
+                    if (two) {
+                        if (kb + 2 <= kb_hi) tmem_ld_x32(tmem + lo + CF::TM_SC + 32 * (kb + 2), ra);
+                        tmem_wait_ld_dep(rb);
+                        weights(kb + 1, rb);
+                    }
+                }
+                // A overlays s, so the blocks above the diagonal block are cleared each time
+                uint32_t z16[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) z16[j] = 0u;
 #pragma unroll 1
                 for (int kb = q4 + 1; kb < 4; ++kb) tmem_st_x16(tmem + lo + CF::TM_A + 16 * kb, z16);
             }
@@ -879,6 +930,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (CF::EPI_ROWS == 32 ? lane == 0 : t == 0) bulk_wait_group_all();
     } else {
         // ============== state conversion: S^T (fp32, TMEM) -> bf16 operand [S | z_hi z_lo] =====
+        // warps 12-15 (V = 64: warps 12-14, the warps whose TMEM lanes hold rows 0..64 of S^T)
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;  // TMEM lane = row of S^T = value index
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
