@@ -393,7 +393,7 @@ struct Cursor {
 enum FwdBar {
     FB_TMA_FULL0 = 0, FB_STAGE_FREE0 = 3, FB_S_FULL = 6, FB_A_FULL, FB_O_FULL0, FB_O_FULL1,
     FB_O_FREE0, FB_O_FREE1, FB_AV_DONE, FB_PHIQ_FULL, FB_PHIQ_FREE, FB_PHIK_FULL, FB_PHIK_FREE,
-    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_DRAIN_B, FB_AV_DONE1, FB_COUNT
+    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_DRAIN_B, FB_AV_DONE1, FB_SBF_FULL1, FB_COUNT
 };
 
 // OBF: the output tile is written as bf16 (round to nearest even from the fp32 quotient) instead
@@ -414,6 +414,12 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + CF::OFF_BAR + 8 * FB_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::OFF_BAR + 8 * FB_COUNT + 4);
     auto BAR = [&](int i) -> uint32_t { return sb + CF::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+    // Conversion k fills state operand buffer k % NSBF and completes a phase of that buffer's
+    // SBF_FULL barrier. With two buffers (V = 64) the state update of the next chunk is issued
+    // before this chunk's read-out, so conversion k + 1 may complete before the read-out waits for
+    // conversion k; one barrier per buffer keeps that waiter within one phase of its barrier.
+    auto sbf_full_bar = [&](int k) -> int { return (CF::NSBF == 2 && (k & 1)) ? FB_SBF_FULL1 : FB_SBF_FULL; };
+    auto sbf_full_par = [&](int k) -> uint32_t { return static_cast<uint32_t>(CF::NSBF == 2 ? (k >> 1) & 1 : k & 1); };
 
     const Part part = cta_range(N, G, blockIdx.x);
     const long long g0 = part.g0, g1 = part.g1;
@@ -446,7 +452,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // STAGE_FREE: one commit from each MMA issuer. V = 64: six warps compute the Taylor
         // weights and three convert the state (see the role split below).
         constexpr uint32_t NW = FAST ? 6 : 4, NC = FAST ? 3 : 4;
-        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, NW, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, NC, NC, 1, 1, 1};
+        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, NW, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, NC, NC, 1, 1, 1, NC};
         for (int i = 0; i < FB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -622,7 +628,9 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     // O += f~(q_c) [S | z_hi z_lo], after O = A [v_c | 1] has completed
                     if (!wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)) return false;
                     if (release_stage >= 0) mma_commit(BAR(FB_STAGE_FREE0 + release_stage));
-                    if (!wait_bar(BAR(FB_SBF_FULL), ro_idx & 1, abort_flag, SITE_SBF_FULL)) return false;
+                    // conversion ro_idx (one SBF_FULL barrier per state operand buffer)
+                    if (!wait_bar(BAR(sbf_full_bar(ro_idx)), sbf_full_par(ro_idx), abort_flag, SITE_SBF_FULL))
+                        return false;
                     const int ob = FAST ? (n & 1) : 0;
                     const uint32_t avp = FAST ? ((n >> 1) & 1) : (n & 1);
                     if (!wait_bar(BAR(ob ? FB_AV_DONE1 : FB_AV_DONE), avp, abort_flag, SITE_AV_DONE))
@@ -971,9 +979,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         };
         auto convert = [&](int cidx, int n) -> bool {
             // SBF_FULL counts one arrival per conversion warp; a warp must not arrive for this
-            // conversion while the previous phase is still open (a warp without rows finishes
-            // early, and the next state update only waits for CONV_READ).
-            if (cidx > 0 && !wait_bar(BAR(FB_SBF_FULL), (cidx - 1) & 1, abort_flag, SITE_SBF_FULL))
+            // conversion while the previous phase of the same barrier is still open (a warp
+            // without rows finishes early, and the next state update only waits for CONV_READ).
+            if (cidx >= CF::NSBF && !wait_bar(BAR(sbf_full_bar(cidx - CF::NSBF)), sbf_full_par(cidx - CF::NSBF),
+                                              abort_flag, SITE_SBF_FULL))
                 return false;
             if (warp == 12 && lane == 0) BASED_TRACE_EV(n, TE_CONV_BEGIN);
             const uint32_t sbf = sb + CF::OFF_SBF + (cidx % CF::NSBF) * CF::SBF;
@@ -1021,7 +1030,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(FB_SBF_FULL));
+            if (lane == 0) mbar_arrive(BAR(sbf_full_bar(cidx)));
             if (warp == 12 && lane == 0) BASED_TRACE_EV(n, TE_CONV_END);
             return true;
         };
