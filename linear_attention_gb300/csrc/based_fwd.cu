@@ -445,12 +445,18 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
         uint16_t *pq = dq + off * K, *pk = dk + off * K, *pv = dv + off * V;
         float *po = dout + off * V;
         off += prow * hp;
-        BASED_CUDA(cudaMemcpy2DAsync(pq, hp * K * 2, q_host + src * K, H * K * 2, hp * K * 2, prow,
-                                     cudaMemcpyHostToDevice, d.hs_in));
-        BASED_CUDA(cudaMemcpy2DAsync(pk, hp * K * 2, k_host + src * K, H * K * 2, hp * K * 2, prow,
-                                     cudaMemcpyHostToDevice, d.hs_in));
-        BASED_CUDA(cudaMemcpy2DAsync(pv, hp * V * 2, v_host + src * V, H * V * 2, hp * V * 2, prow,
-                                     cudaMemcpyHostToDevice, d.hs_in));
+        // A piece of whole batch entries is one contiguous block: copy it as such (the 2D path
+        // moves short rows, such as 192-byte q rows, far below the link's bandwidth).
+        const bool whole = hp == H;
+        auto copy_in = [&](uint16_t *dst, const uint16_t *hsrc, int dim) -> cudaError_t {
+            const size_t w = static_cast<size_t>(hp) * dim * 2;
+            return whole ? cudaMemcpyAsync(dst, hsrc + src * dim, prow * w, cudaMemcpyHostToDevice, d.hs_in)
+                         : cudaMemcpy2DAsync(dst, w, hsrc + src * dim, static_cast<size_t>(H) * dim * 2, w, prow,
+                                             cudaMemcpyHostToDevice, d.hs_in);
+        };
+        BASED_CUDA(copy_in(pq, q_host, K));
+        BASED_CUDA(copy_in(pk, k_host, K));
+        BASED_CUDA(copy_in(pv, v_host, V));
         BASED_CUDA(cudaEventRecord(d.hin[i], d.hs_in));
         BASED_CUDA(cudaStreamWaitEvent(d.hs_comp, d.hin[i], 0));
         rc = run(pq, pk, pv, pb, T, hp, K, V, scale, po, false, wsb, ws_piece, false,
@@ -458,8 +464,12 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
         if (rc != BASED_OK) return rc;
         BASED_CUDA(cudaEventRecord(d.hcomp[i], d.hs_comp));
         BASED_CUDA(cudaStreamWaitEvent(d.hs_out, d.hcomp[i], 0));
-        BASED_CUDA(cudaMemcpy2DAsync(o_host + src * V, H * V * 4, po, hp * V * 4, hp * V * 4, prow,
-                                     cudaMemcpyDeviceToHost, d.hs_out));
+        if (whole)
+            BASED_CUDA(cudaMemcpyAsync(o_host + src * V, po, prow * hp * V * 4, cudaMemcpyDeviceToHost, d.hs_out));
+        else
+            BASED_CUDA(cudaMemcpy2DAsync(o_host + src * V, static_cast<size_t>(H) * V * 4, po,
+                                         static_cast<size_t>(hp) * V * 4, static_cast<size_t>(hp) * V * 4, prow,
+                                         cudaMemcpyDeviceToHost, d.hs_out));
     }
     // join: the caller's stream continues after the last copy out, then the call waits for it
     BASED_CUDA(cudaEventRecord(d.hdone, d.hs_out));
