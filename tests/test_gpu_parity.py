@@ -211,3 +211,28 @@ def test_bounded_wait_reports_timeout_without_hanging(cuda_device):
     q, k, v = [t.to(cuda_device) for t in make_inputs(1, 256, 2, 8, 64, 35)]
     based_fwd(q, k, v)  # the context is still usable afterwards
     torch.cuda.synchronize()
+
+
+def test_calls_replay_from_a_cuda_graph(cuda_device):
+    """After a warm-up call (which sizes the library workspace), based_fwd calls can be captured
+    into a CUDA graph, programmatic-dependent launches included, and replayed bit for bit."""
+    shapes = [(4, 4096, 16, 16, 64, 40), (1, 2048, 8, 8, 128, 41), (2, 1500, 3, 16, 128, 42)]
+    cases = []
+    for B, T, H, K, V, seed in shapes:
+        q, k, v = [t.to(cuda_device) for t in make_inputs(B, T, H, K, V, seed)]
+        ref = based_fwd(q, k, v)  # eager result (and warm-up)
+        cases.append((q, k, v, ref, torch.empty_like(ref)))
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(cuda_device)
+    s.wait_stream(torch.cuda.current_stream(cuda_device))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for q, k, v, _, out in cases:
+            based_fwd(q, k, v, out=out, stream=s)
+    for _ in range(2):
+        for *_, out in cases:
+            out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for q, k, v, ref, out in cases:
+            assert torch.equal(out, ref)
