@@ -1386,15 +1386,24 @@ __global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems,
     const int vec = slot_elems / 4;  // slots are whole float4s
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < vec; e += gridDim.x * blockDim.x) {
         float4 *p = reinterpret_cast<float4 *>(slots + static_cast<size_t>(i0) * slot_elems) + e;
-        float4 acc = *p;
-        for (int j = 1; j < len; ++j) {
-            p += vec;
-            const float4 x = *p;
-            acc.x += x.x;
-            acc.y += x.y;
-            acc.z += x.z;
-            acc.w += x.w;
-            *p = acc;
+        float4 acc = p[0];
+        // up to four slots per step, their loads issued together (one round trip instead of one per
+        // slot); the sums stay in range order
+        for (int j0 = 1; j0 < len; j0 += 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j0 + u < len) x[u] = p[static_cast<size_t>(j0 + u) * vec];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j0 + u < len) {
+                    acc.x += x[u].x;
+                    acc.y += x[u].y;
+                    acc.z += x[u].z;
+                    acc.w += x[u].w;
+                    p[static_cast<size_t>(j0 + u) * vec] = acc;
+                }
+            }
         }
     }
 }
