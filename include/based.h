@@ -116,9 +116,11 @@ BASED_API int based_fwd_bf16_out(const uint16_t *q, const uint16_t *k, const uin
  *   partial states) lives in one fixed array of BASED_NOALLOC_SCRATCH_BYTES bytes that is part of
  *   the library's device image: every GPU that loads the library holds it until process exit.
  *   The call itself runs no cudaMalloc, cudaFree or other allocating routine.
- *   - Shapes whose scratch would exceed the array are rejected with BASED_ERR_SCRATCH_LIMIT
- *     before anything is launched (based_fwd_workspace_size() tells the need; for K = 16,
- *     V = 128 it is 82,560 bytes per SM, so 16 MiB covers up to 203 SMs).
+ *   - The work plan is limited to what fits the array: where based_fwd would cut the aggregate
+ *     pass into more pieces (one partial-state slot each) than fit, this entry point keeps one
+ *     slot per range (82,560 bytes per SM for K = 16, V = 128, so 16 MiB covers up to 203 SMs).
+ *     Shapes whose scratch would still exceed the array are rejected with
+ *     BASED_ERR_SCRATCH_LIMIT before anything is launched.
  *   - The first call on a device looks up the array's device address (and loads the library's
  *     device code there if that has not happened yet); make that first call before any stream
  *     capture.

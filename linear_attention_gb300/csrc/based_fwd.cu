@@ -86,8 +86,7 @@ struct Plan {
     bool need_agg;  // some range ends inside a head
     int slot_floats;
     size_t ws_bytes;
-    ScanRuns runs;  // runs of ranges whose partial states chain into one head's prefix
-    bool scan;      // some prefix chains more than kMaxChain partial states: run the scan kernel
+    AggPlan agg;    // pieces of the aggregate pass, the forward CTAs' prefixes, the scan runs
 };
 
 constexpr int kMaxDevices = 64;
@@ -131,7 +130,9 @@ int current_device(int *dev) {
 
 int slot_floats(int K, int V) { return (V + 1) * ((K == 16) ? 160 : 48); }
 
-Plan make_plan(int B, int T, int H, int K, int V, int sms) {
+// max_ws: workspace bytes the plan may use at most (the balanced aggregate pass needs a slot per
+// piece, up to about twice the ranges; with less it falls back to one slot per range)
+Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~static_cast<size_t>(0)) {
     Plan p;
     p.n_c = (T + kChunk - 1) / kChunk;
     p.N = static_cast<long long>(B) * H * p.n_c;
@@ -140,12 +141,11 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms) {
     p.need_agg = false;
     for (int i = 0; i < p.G; ++i)
         if (has_aggregate(p.N, p.G, i, p.n_c)) p.need_agg = true;
-    p.runs = make_scan_runs(p.N, p.G, p.n_c);
-    p.scan = false;
-    for (int r = 0; r < p.runs.n; ++r)
-        if (p.runs.len[r] > kMaxChain) p.scan = true;
     p.slot_floats = slot_floats(K, V);
-    p.ws_bytes = p.need_agg ? static_cast<size_t>(p.G) * p.slot_floats * sizeof(float) : 0;
+    const size_t slot_bytes = static_cast<size_t>(p.slot_floats) * sizeof(float);
+    const size_t max_slots = max_ws / slot_bytes;
+    make_agg_plan(p.N, p.G, p.n_c, p.G, max_slots < kMaxPieces ? static_cast<int>(max_slots) : kMaxPieces, p.agg);
+    p.ws_bytes = p.need_agg ? static_cast<size_t>(p.agg.pieces.n) * slot_bytes : 0;
     return p;
 }
 
@@ -216,12 +216,15 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
         BASED_OK)
         return rc;
     if (p.need_agg) {
-        based_agg_kernel<K, V><<<p.G, kAggThreads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.N, p.G);
+        // 512 threads (dedicated slot writers) when a CTA sums several pieces, else 384
+        const int threads = p.agg.pieces.n > p.agg.pieces.n_cta ? kAggThreads : 384;
+        based_agg_kernel<K, V><<<p.agg.pieces.n_cta, threads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c,
+                                                                              p.agg.pieces);
         BASED_CUDA(cudaGetLastError());
-        if (p.scan) {  // otherwise each forward CTA sums the (at most kMaxChain) states it needs
-            dim3 grid((p.slot_floats / 4 + 255) / 256, p.runs.n);
+        if (p.agg.scan) {  // otherwise each forward CTA sums the (at most kMaxChain) slots it needs
+            dim3 grid((p.slot_floats / 4 + 255) / 256, p.agg.runs.n);
             BASED_CUDA(launch_dependent(based_scan_kernel, grid, dim3(256), 0, st, true, ws,
-                                        p.slot_floats, p.runs));
+                                        p.slot_floats, p.agg.runs));
         }
     }
     if (ev_begin) BASED_CUDA(cudaEventRecord(ev_begin, st));
@@ -232,21 +235,22 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     const bool dependent = p.need_agg && !ev_begin;
     BASED_CUDA(launch_dependent(based_fwd_kernel<K, V, OBF>, dim3(p.G), dim3(kFwdThreads), CF::SMEM_FWD, st,
                                 dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
-                                p.N, p.G, scale, p.scan ? 1 : kMaxChain));
+                                p.N, p.G, scale, p.agg.pre));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }
 
 // obf: o holds bf16 (else fp32)
+// max_ws: the most workspace the plan may use (the fixed scratch of based_fwd_noalloc)
 int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, int H, int K, int V,
         float scale, void *o, bool obf, void *ws, size_t ws_bytes, bool own_ws, based_stream_t stream,
-        void *ev_begin = nullptr, void *ev_end = nullptr) {
+        void *ev_begin = nullptr, void *ev_end = nullptr, size_t max_ws = ~static_cast<size_t>(0)) {
     int rc = check_args(q, k, v, B, T, H, K, V, o, obf ? 2 : 4);
     if (rc != BASED_OK) return rc;
     int dev;
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
     DeviceState &d = g_dev[dev];
-    const Plan p = make_plan(B, T, H, K, V, d.sms);
+    const Plan p = make_plan(B, T, H, K, V, d.sms, max_ws);
     if (!(scale > 0.0f) || std::isnan(scale)) scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
     if (own_ws) {
         std::lock_guard<std::mutex> lk(d.m);
@@ -326,11 +330,13 @@ int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
     if (rc != BASED_OK) return rc;
     int dev;
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
-    const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms);
+    // the plan that fits the fixed scratch (one slot per range when balanced pieces do not fit)
+    const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms, BASED_NOALLOC_SCRATCH_BYTES);
     if (p.ws_bytes > BASED_NOALLOC_SCRATCH_BYTES) return BASED_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     if (p.ws_bytes > 0 && (rc = noalloc_scratch(dev, &scratch)) != BASED_OK) return rc;
-    return run(q, k, v, B, T, H, K, V, scale, o, false, scratch, p.ws_bytes, false, stream);
+    return run(q, k, v, B, T, H, K, V, scale, o, false, scratch, p.ws_bytes, false, stream, nullptr,
+               nullptr, BASED_NOALLOC_SCRATCH_BYTES);
 }
 
 int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
@@ -338,7 +344,7 @@ int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
     int dev;
     if (current_device(&dev) != BASED_OK) return 0;
     const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms);
-    return p.need_agg ? (p.scan ? 3 : 2) : 1;
+    return p.need_agg ? (p.agg.scan ? 3 : 2) : 1;
 }
 
 size_t based_fwd_workspace_size(int B, int T, int H, int K, int V) {

@@ -26,7 +26,7 @@ namespace based {
 constexpr int kChunk = 128;            // rows per chunk = MMA M
 constexpr int kMaxChain = 2;           // partial states a forward CTA sums into its prefix itself
 constexpr int kFwdThreads = 512;       // 4 warpgroups
-constexpr int kAggThreads = 384;       // 3 warpgroups
+constexpr int kAggThreads = 512;       // 4 warpgroups
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after 1 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // drain of in-flight copies after an abort
 
@@ -61,7 +61,7 @@ enum TraceEvent {
 enum WaitSite : uint32_t {
     SITE_STAGE_FREE = 1, SITE_TMA_FULL, SITE_S_FULL, SITE_A_FULL, SITE_O_FULL, SITE_O_FREE,
     SITE_AV_DONE, SITE_PHIQ_FULL, SITE_PHIQ_FREE, SITE_PHIK_FULL, SITE_PHIK_FREE, SITE_UPD_DONE,
-    SITE_SBF_FULL, SITE_CONV_READ, SITE_AGG_DONE, SITE_DRAIN, SITE_SELFTEST = 255
+    SITE_SBF_FULL, SITE_CONV_READ, SITE_AGG_DONE, SITE_DRAIN, SITE_SLOT_READ, SITE_SELFTEST = 255
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t site) {
@@ -351,6 +351,155 @@ __host__ __device__ __forceinline__ int prefix_chain_len(long long N, int G, int
     return m;
 }
 
+// ------------------------------------------------------------------------------------------------
+// Work plan of the aggregate pass (host side; also used by the partition check)
+// ------------------------------------------------------------------------------------------------
+constexpr int kMaxRanges = 256;             // upper bound on G (one range per SM)
+constexpr int kMaxPieces = 2 * kMaxRanges;  // stretches + aggregate-CTA boundaries inside them
+
+// The stretches (the last stretch of every range that ends inside a head), concatenated in range
+// order and cut into n_cta segments of equal length, one per aggregate CTA, so that no CTA waits
+// on a long stretch while others idle. A segment's part in one stretch is a piece; each piece's
+// partial state has its own slot (slot index = piece index, pieces in concatenated order).
+struct AggPieces {
+    int n_cta;                           // aggregate CTAs
+    int n;                               // pieces (= slots)
+    uint16_t cta_first[kMaxRanges + 1];  // CTA j sums pieces [cta_first[j], cta_first[j + 1])
+    int32_t g0[kMaxPieces];              // first chunk (global chunk index) of each piece
+    int32_t len[kMaxPieces];             // chunks of each piece
+};
+// Prefix of forward CTA r: the sum of slots slot[r] .. slot[r] + cnt[r] - 1 (cnt = 0: the range
+// starts at a head start and needs none).
+struct Prefixes {
+    uint16_t slot[kMaxRanges];
+    uint8_t cnt[kMaxRanges];
+};
+// Runs of slots that a scan turns into inclusive prefixes: one per chain of stretches in a head
+// with two or more pieces.
+struct ScanRuns {
+    int n;                         // number of runs
+    uint16_t start[kMaxRanges];    // first slot of the run
+    uint16_t len[kMaxRanges];      // slots in the run (>= 2)
+};
+struct AggPlan {
+    AggPieces pieces;
+    Prefixes pre;
+    ScanRuns runs;
+    bool scan;  // some prefix has more than kMaxChain slots: the scan kernel runs, every cnt is 1
+};
+
+// Completes a plan whose pieces are set: the prefix of every range that starts inside a head (the
+// pieces of the chain of stretches before it in that head) and, when some prefix has more than
+// kMaxChain pieces, the scan runs (one per chain of two or more pieces; each prefix is then the
+// last slot of its chain's part of the run).
+inline void finish_agg_plan(long long N, int G, int n_c, int ns, const int *st_range, const int *first_piece,
+                            const int *last_piece, AggPlan &P) {
+    int stretch_of[kMaxRanges], last_of[kMaxRanges];
+    for (int i = 0; i < G; ++i) stretch_of[i] = -1;
+    for (int s = 0; s < ns; ++s) stretch_of[st_range[s]] = s;
+    P.scan = false;
+    for (int r = 0; r < G; ++r) {
+        P.pre.cnt[r] = 0;
+        P.pre.slot[r] = 0;
+        last_of[r] = -1;
+        if (cta_range(N, G, r).g0 % n_c == 0) continue;
+        const int m = prefix_chain_len(N, G, r, n_c, G);
+        const int f = first_piece[stretch_of[r - m]], l = last_piece[stretch_of[r - 1]];
+        P.pre.slot[r] = static_cast<uint16_t>(f);
+        P.pre.cnt[r] = static_cast<uint8_t>(l - f + 1 < 255 ? l - f + 1 : 255);
+        last_of[r] = l;
+        if (l - f + 1 > kMaxChain) P.scan = true;
+    }
+    P.runs.n = 0;
+    if (!P.scan) return;
+    for (int s = 0; s < ns; ++s) {
+        if (continues_prefix(N, G, st_range[s], n_c)) continue;
+        int t = s + 1;
+        while (t < ns && st_range[t] == st_range[t - 1] + 1 && continues_prefix(N, G, st_range[t], n_c)) ++t;
+        const int f = first_piece[s], l = last_piece[t - 1];
+        if (l - f + 1 >= 2) {
+            P.runs.start[P.runs.n] = static_cast<uint16_t>(f);
+            P.runs.len[P.runs.n] = static_cast<uint16_t>(l - f + 1);
+            ++P.runs.n;
+        }
+    }
+    for (int r = 0; r < G; ++r)
+        if (P.pre.cnt[r] > 0) {
+            P.pre.slot[r] = static_cast<uint16_t>(last_of[r]);
+            P.pre.cnt[r] = 1;
+        }
+}
+
+// Builds the plan for G ranges over N chunks (n_c per head). Two candidates: one aggregate CTA per
+// stretch, or the stretches cut evenly over up to max_cta CTAs (only if it needs at most max_slots
+// slots). The balanced cut is taken when its estimated critical path, in chunks of aggregate work,
+// is clearly shorter: the longest CTA load, plus about two chunks for the extra pieces' slot
+// writes, plus about six when the plan needs the scan kernel (measured on GB300: an aggregate
+// chunk takes about 0.5 us, the scan and its launch about 3 us).
+inline void make_agg_plan(long long N, int G, int n_c, int max_cta, int max_slots, AggPlan &P) {
+    int ns = 0;
+    int st_range[kMaxRanges];
+    long long st_g0[kMaxRanges], st_len[kMaxRanges], L = 0, longest = 0;
+    for (int i = 0; i < G; ++i) {
+        if (!has_aggregate(N, G, i, n_c)) continue;
+        const Part p = cta_range(N, G, i);
+        const long long hs = ((p.g1 - 1) / n_c) * n_c;
+        const long long ga = p.g0 > hs ? p.g0 : hs;
+        st_range[ns] = i;
+        st_g0[ns] = ga;
+        st_len[ns] = p.g1 - ga;
+        L += st_len[ns];
+        longest = st_len[ns] > longest ? st_len[ns] : longest;
+        ++ns;
+    }
+    int first_piece[kMaxRanges], last_piece[kMaxRanges];
+    // one aggregate CTA per stretch
+    AggPieces &A = P.pieces;
+    A.n_cta = ns;
+    for (int s = 0; s < ns; ++s) {
+        A.cta_first[s] = static_cast<uint16_t>(s);
+        A.g0[s] = static_cast<int32_t>(st_g0[s]);
+        A.len[s] = static_cast<int32_t>(st_len[s]);
+        first_piece[s] = last_piece[s] = s;
+    }
+    A.cta_first[ns] = static_cast<uint16_t>(ns);
+    A.n = ns;
+    finish_agg_plan(N, G, n_c, ns, st_range, first_piece, last_piece, P);
+    const int cap = max_cta < kMaxRanges ? max_cta : kMaxRanges;
+    const int n_cta = static_cast<int>(L < cap ? L : cap);
+    if (ns == 0 || n_cta <= ns) return;
+    constexpr long long kPiecePenalty = 2, kScanPenalty = 6;
+    const long long cost_one = longest + (P.scan ? kScanPenalty : 0);
+    const long long bal_load = (L + n_cta - 1) / n_cta;
+    if (10 * (bal_load + kPiecePenalty) >= 85 * cost_one / 10) return;  // no clear gain even without a scan
+    // the balanced cut: CTA j sums concatenated positions [L j / n_cta, L (j + 1) / n_cta)
+    static thread_local AggPlan B;
+    int bfirst[kMaxRanges], blast[kMaxRanges];
+    int n = 0, s = 0;
+    long long s_off = 0;  // concatenated offset of stretch s
+    B.pieces.n_cta = n_cta;
+    for (int j = 0; j < n_cta; ++j) {
+        const long long x1 = L * (j + 1) / n_cta;
+        B.pieces.cta_first[j] = static_cast<uint16_t>(n);
+        for (long long x = L * j / n_cta; x < x1;) {
+            while (x >= s_off + st_len[s]) s_off += st_len[s++];
+            const long long end = x1 < s_off + st_len[s] ? x1 : s_off + st_len[s];
+            if (n >= kMaxPieces || n >= max_slots) return;  // keep one CTA per stretch
+            B.pieces.g0[n] = static_cast<int32_t>(st_g0[s] + (x - s_off));
+            B.pieces.len[n] = static_cast<int32_t>(end - x);
+            if (x == s_off) bfirst[s] = n;
+            blast[s] = n;
+            ++n;
+            x = end;
+        }
+    }
+    B.pieces.cta_first[n_cta] = static_cast<uint16_t>(n);
+    B.pieces.n = n;
+    finish_agg_plan(N, G, n_c, ns, st_range, bfirst, blast, B);
+    const long long cost_bal = bal_load + kPiecePenalty + (B.scan ? kScanPenalty : 0);
+    if (100 * cost_bal < 85 * cost_one) P = B;
+}
+
 // Walks the chunks of a range without divisions: (b, h, c) advance like an odometer.
 struct Cursor {
     int n, last, c, h, b, n_c, H;
@@ -403,7 +552,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G,
-                 float scale, int max_chain) {
+                 float scale, const __grid_constant__ Prefixes pre) {
     using CF = Cfg<K, V>;
     constexpr bool FAST = CF::FAST;
     extern __shared__ uint8_t smem_raw[];
@@ -1038,11 +1187,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         int cidx = 0;
         // A range that starts inside a head continues from the prefix state of the chunks before
         // it: load it into TMEM, then convert it like any other state.
-        if (g0 % n_c != 0) {
-            // The prefix is the sum of the partial states of the ranges since the head's last
-            // range boundary that starts a stretch: slots blockIdx - m .. blockIdx - 1 (m <= max_chain;
-            // max_chain = 1 when a scan has already summed them into slot blockIdx - 1).
-            const int m = prefix_chain_len(N, G, static_cast<int>(blockIdx.x), n_c, max_chain);
+        if (pre.cnt[blockIdx.x] > 0) {
+            // The prefix is the sum of the partial states of the pieces of the head before this
+            // range: slots pre.slot .. pre.slot + m - 1 (m <= kMaxChain; m = 1 when a scan has
+            // already summed them).
+            const int m = pre.cnt[blockIdx.x];
             // launched as a dependent of the aggregate / scan kernel: only this read of their
             // output waits for them (every other role starts right away)
             griddep_wait();
@@ -1050,7 +1199,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (r == 0 && trace_buf_ != nullptr)
                 trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 24] = global_timer_ns();
 #endif
-            const float *slot = prefix + static_cast<size_t>(blockIdx.x - m) * CF::SLOT;
+            const float *slot = prefix + static_cast<size_t>(pre.slot[blockIdx.x]) * CF::SLOT;
             // One code path per chain length, so that every load it issues is needed and all of a
             // step's loads are in flight together; the terms are summed in range order.
             auto load_prefix = [&](auto chain_len) {
@@ -1122,24 +1271,57 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }
 
 // ------------------------------------------------------------------------------------------------
-// Aggregate kernel: the partial state [S^T | z] of the last stretch of a range that ends inside a
-// head, written as fp32 rows into slot blockIdx.x.
-// warp 0: TMA producer | warp 1: MMA issuer | warps 2-3: idle | warps 4-11: f(k) tiles (half of
-// each token row per warp), then warps 8-11 write the slot
+// Aggregate kernel: the partial states [S^T | z] of the pieces of the stretches (the last stretch
+// of every range that ends inside a head), each written as fp32 into its slot. CTA j sums the
+// chunks of pieces cta_first[j] .. cta_first[j + 1] - 1 in order, into two TMEM accumulators used
+// in turn, so that one piece's slot is written while the next piece is summed.
+// warp 0: TMA producer | warp 1: MMA issuer | warp 2: owns TMEM | warp 3: idle | warps 4-11: f(k)
+// tiles (half of each token row per warp) | warps 12-15: slot writers (512 threads; with 384, one
+// piece per CTA, warps 8-11 write the slot after building)
 // ------------------------------------------------------------------------------------------------
 // Barriers of the aggregate kernel with S k/v stages and NP f(k) buffers: TMA_FULL[S],
-// STAGE_FREE[S], PHIK_FULL[NP], PHIK_FREE[NP], AGG_DONE.
+// STAGE_FREE[S], PHIK_FULL[NP], PHIK_FREE[NP], per accumulator AGG_DONE[2] (its piece is summed)
+// and SLOT_READ[2] (its slot is written), DRAIN.
 template <int S, int NP>
 struct AggBar {
     static constexpr int TMA_FULL0 = 0, STAGE_FREE0 = S, PHIK_FULL0 = 2 * S, PHIK_FREE0 = 2 * S + NP,
-                         AGG_DONE = 2 * S + 2 * NP, COUNT = 2 * S + 2 * NP + 1;
+                         AGG_DONE0 = 2 * S + 2 * NP, SLOT_READ0 = AGG_DONE0 + 2, DRAIN = SLOT_READ0 + 2,
+                         COUNT = DRAIN + 1;
     static_assert(8 * COUNT + 8 <= 256, "barrier area");
+};
+constexpr uint32_t kAggAccStride = 256;  // TMEM columns between the two accumulators
+
+// Walks the chunks of pieces p .. p_end - 1 in order.
+struct PieceWalk {
+    Cursor cu;
+    const AggPieces *ap;
+    int p, p_end, j, n_c, H;
+    __device__ __forceinline__ void init(const AggPieces &a, int p0, int p1, int n_c_, int H_) {
+        ap = &a;
+        p = p0;
+        p_end = p1;
+        j = 0;
+        n_c = n_c_;
+        H = H_;
+        if (p < p_end) cu.init(a.g0[p], a.len[p], n_c, H);
+    }
+    __device__ __forceinline__ bool done() const { return p >= p_end; }
+    __device__ __forceinline__ bool first() const { return j == 0; }
+    __device__ __forceinline__ bool last() const { return j == ap->len[p] - 1; }
+    __device__ __forceinline__ void next() {
+        if (++j == ap->len[p]) {
+            j = 0;
+            if (++p < p_end) cu.init(ap->g0[p], ap->len[p], n_c, H);
+        } else {
+            cu.next();
+        }
+    }
 };
 
 template <int K, int V>
 __global__ void __launch_bounds__(kAggThreads, 1)
 based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 float *__restrict__ slots, int H, int n_c, long long N, int G) {
+                 float *__restrict__ slots, int H, int n_c, const __grid_constant__ AggPieces ap) {
     using CF = Cfg<K, V>;
     constexpr int S = CF::A_NST;
     constexpr int NP = CF::A_NPHIK;
@@ -1149,12 +1331,13 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     griddep_launch_dependents();
     constexpr int AB_TMA_FULL0 = AB::TMA_FULL0, AB_STAGE_FREE0 = AB::STAGE_FREE0,
                   AB_PHIK_FULL0 = AB::PHIK_FULL0, AB_PHIK_FREE0 = AB::PHIK_FREE0,
-                  AB_AGG_DONE = AB::AGG_DONE, AB_COUNT = AB::COUNT;
-    if (!has_aggregate(N, G, blockIdx.x, n_c)) return;
-    const Part part = cta_range(N, G, blockIdx.x);
-    const long long ga = part.g0 > ((part.g1 - 1) / n_c) * n_c ? part.g0 : ((part.g1 - 1) / n_c) * n_c;
-    const long long g1 = part.g1;
-    const int nchunks = static_cast<int>(g1 - ga);
+                  AB_AGG_DONE0 = AB::AGG_DONE0, AB_SLOT_READ0 = AB::SLOT_READ0, AB_DRAIN = AB::DRAIN,
+                  AB_COUNT = AB::COUNT;
+    if (static_cast<int>(blockIdx.x) >= ap.n_cta) return;
+    const int p0 = ap.cta_first[blockIdx.x], p1 = ap.cta_first[blockIdx.x + 1];
+    int nchunks = 0;
+    for (int p = p0; p < p1; ++p) nchunks += ap.len[p];
+    if (nchunks <= 0) return;
 
     extern __shared__ uint8_t smem_raw[];
     BASED_TRACE_INIT;
@@ -1170,11 +1353,11 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::A_OFF_BAR + 8 * AB_COUNT + 4);
     auto BAR = [&](int i) -> uint32_t { return sb + CF::A_OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
-    // k, v tiles of stretch chunk n (cursor position cu) into stage n % S, completing on TMA_FULL
-    auto issue_loads = [&](int n, const Cursor &cu) {
-        const int s = n % S;
+    // k, v tiles of the CTA's chunk u (cursor position cu) into stage u % S, completing on TMA_FULL
+    auto issue_loads = [&](int u, const Cursor &cu) {
+        const int s = u % S;
         const uint32_t bar = BAR(AB_TMA_FULL0 + s);
-        BASED_TRACE_EV(n + 40, 0);
+        BASED_TRACE_EV(u + 40, 0);
         mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
         tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
         tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
@@ -1183,19 +1366,22 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     };
     const int n_early = nchunks < S ? nchunks : S;  // loads issued during set-up
     if (threadIdx.x == 0) {
-        for (int i = 0; i < AB_COUNT; ++i)
-            mbar_init(BAR(i), (i >= AB_PHIK_FULL0 && i < AB_PHIK_FULL0 + NP) ? 8u : 1u);
+        for (int i = 0; i < AB_COUNT; ++i) {
+            const bool phik_full = i >= AB_PHIK_FULL0 && i < AB_PHIK_FULL0 + NP;
+            const bool slot_read = i >= AB_SLOT_READ0 && i < AB_SLOT_READ0 + 2;
+            mbar_init(BAR(i), phik_full ? 8u : (slot_read ? 4u : 1u));
+        }
         *abort_flag = 0;
         fence_mbar_init();
         // the first loads go out now (this thread is the TMA producer)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
-        Cursor cu;
-        cu.init(ga, nchunks, n_c, H);
-        for (int n = 0; n < n_early; ++n, cu.next()) issue_loads(n, cu);
+        PieceWalk w;
+        w.init(ap, p0, p1, n_c, H);
+        for (int u = 0; u < n_early; ++u, w.next()) issue_loads(u, w.cu);
     }
     if constexpr (CF::ZROW) {
-        for (int i = threadIdx.x; i < CF::ONES / 16; i += kAggThreads)
+        for (int i = threadIdx.x; i < CF::ONES / 16; i += blockDim.x)
             st_shared_v4(sb + CF::A_OFF_ONES + 16u * i, 0u, 0u, 0u, 0u);
         __syncthreads();
         if (threadIdx.x < 16)
@@ -1205,8 +1391,10 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         st_shared_v4(sb + CF::A_OFF_ZONES + 16u * threadIdx.x, threadIdx.x < 2 ? 0x3F803F80u : 0u,
                      threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u,
                      threadIdx.x < 2 ? 0x3F803F80u : 0u);
+    // one accumulator (256 columns) when the CTA sums one piece, else two
+    const uint32_t tmem_cols = p1 - p0 > 1 ? 2 * kAggAccStride : kAggAccStride;
     if (warp == 2) {
-        tmem_alloc(smem_u32(tmem_holder), 256);
+        tmem_alloc(smem_u32(tmem_holder), tmem_cols);
         tmem_relinquish();
     }
     fence_proxy_async_smem();
@@ -1218,14 +1406,14 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (warp == 0) {
         if (lane == 0) {
             int issued = n_early;
-            Cursor cu;
-            cu.init(ga, nchunks, n_c, H);
-            for (int n = 0; n < n_early; ++n) cu.next();
-            for (int n = n_early; n < nchunks; ++n, cu.next()) {
-                const int s = n % S;
-                if (!wait_bar(BAR(AB_STAGE_FREE0 + s), ((n / S) - 1) & 1, abort_flag, SITE_STAGE_FREE))
+            PieceWalk w;
+            w.init(ap, p0, p1, n_c, H);
+            for (int u = 0; u < n_early; ++u) w.next();
+            for (int u = n_early; u < nchunks; ++u, w.next()) {
+                const int s = u % S;
+                if (!wait_bar(BAR(AB_STAGE_FREE0 + s), ((u / S) - 1) & 1, abort_flag, SITE_STAGE_FREE))
                     break;
-                issue_loads(n, cu);
+                issue_loads(u, w.cu);
                 ++issued;
             }
             if (*abort_flag) {
@@ -1239,20 +1427,28 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t ID_UPD = idesc_bf16_f32(128, CF::PP, 1, 1);
             constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
-            const uint32_t t_s = tmem, t_z = tmem + CF::TA_Z;
             const uint64_t d_zones = smem_desc(sb + CF::A_OFF_ZONES, 16, 256, LAYOUT_SW32);
-            for (int n = 0; n < nchunks; ++n) {
-                const int s = n % S, pb = n % NP;
-                if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
-                if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (n / NP) & 1, abort_flag, SITE_PHIK_FULL)) break;
-                BASED_TRACE_EV(n + 40, 1);
+            PieceWalk w;
+            w.init(ap, p0, p1, n_c, H);
+            int kk = 0;  // pieces of this CTA started
+            for (int u = 0; u < nchunks; ++u, w.next()) {
+                const int s = u % S, pb = u % NP, b = kk & 1;
+                // accumulator b is free once the slot of the piece two before was written
+                if (w.first() && kk >= 2 &&
+                    !wait_bar(BAR(AB_SLOT_READ0 + b), ((kk - 2) >> 1) & 1, abort_flag, SITE_SLOT_READ))
+                    break;
+                if (!wait_bar(BAR(AB_TMA_FULL0 + s), (u / S) & 1, abort_flag, SITE_TMA_FULL)) break;
+                if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (u / NP) & 1, abort_flag, SITE_PHIK_FULL)) break;
+                BASED_TRACE_EV(u + 40, 1);
                 tc_fence_after();
+                const uint32_t t_s = tmem + b * kAggAccStride, t_z = t_s + CF::TA_Z;
                 const uint32_t lbo_a = CF::ZROW ? (CF::A_OFF_ONES - (CF::A_OFF_V + s * CF::VT)) : 16384u;
                 const uint64_t d_va = smem_desc(sb + CF::A_OFF_V + s * CF::VT, lbo_a, 1024, LAYOUT_SW128);
                 const uint64_t d_phik = smem_desc(sb + CF::A_OFF_PHIK + pb * CF::PHI, 4096, 256, LAYOUT_SW32);
+                const bool carry = !w.first();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint32_t acc = (j > 0 || n > 0) ? 1u : 0u;
+                    const uint32_t acc = (j > 0 || carry) ? 1u : 0u;
                     mma_ss(t_s, v_step<CF::ZROW>(d_va, j), dadd(d_phik, 512 * j), ID_UPD, acc);
                     if constexpr (!CF::ZROW) {
                         mma_ss(t_z, dadd(d_phik, 512 * j), d_zones, ID_Z, acc);
@@ -1262,50 +1458,62 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 }
                 mma_commit(BAR(AB_PHIK_FREE0 + pb));
                 mma_commit(BAR(AB_STAGE_FREE0 + s));
-                BASED_TRACE_EV(n + 40, 2);
+                if (w.last()) {
+                    mma_commit(BAR(AB_AGG_DONE0 + b));  // piece kk summed
+                    ++kk;
+                }
+                BASED_TRACE_EV(u + 40, 2);
             }
-            mma_commit(BAR(AB_AGG_DONE));
-            wait_bar(BAR(AB_AGG_DONE), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
+            // every MMA issued must finish before TMEM is released
+            mma_commit(BAR(AB_DRAIN));
+            wait_bar(BAR(AB_DRAIN), 0, nullptr, SITE_DRAIN, kDrainLimitNs);
         }
     } else if (warp < 4) {
         // warps 2 and 3: no role (warp 2 owns the TMEM allocation)
-    } else {
+    } else if (warp < 12) {
         // feature builders (warps 4-11): token t of the chunk, warps 4-7 the first half of its
         // feature blocks and warps 8-11 the second half, cycling through the f(k) buffers
         const int t = (warp & 3) * 32 + lane;
         const int f_lo = warp < 8 ? 0 : (CF::NBLK + 1) / 2, f_hi = warp < 8 ? (CF::NBLK + 1) / 2 : CF::NBLK;
-        for (int n = 0; n < nchunks; ++n) {
-            const int s = n % S, pb = n % NP;
-            if (!wait_bar(BAR(AB_TMA_FULL0 + s), (n / S) & 1, abort_flag, SITE_TMA_FULL)) break;
-            if (n >= NP && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((n / NP) - 1) & 1, abort_flag,
+        for (int u = 0; u < nchunks; ++u) {
+            const int s = u % S, pb = u % NP;
+            if (!wait_bar(BAR(AB_TMA_FULL0 + s), (u / S) & 1, abort_flag, SITE_TMA_FULL)) break;
+            if (u >= NP && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((u / NP) - 1) & 1, abort_flag,
                                      SITE_PHIK_FREE))
                 break;
-            if (warp == 4 && lane == 0) BASED_TRACE_EV(n + 40, 3);
+            if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 3);
             build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
                               kBf16One2, kBf16One2, f_lo, f_hi);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
-            if (warp == 4 && lane == 0) BASED_TRACE_EV(n + 40, 4);
+            if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 4);
         }
     }
-    if (warp >= 8) {
-        // writer (warps 8-11, after building): S^T rows (and z) -> fp32 slot
+    // Slot writers: S^T rows (and z) of each summed piece -> its fp32 slot, element (c, r) at
+    // c * SROWS + r. With several pieces per CTA they are warps 12-15 (512 threads), so that the
+    // f(k) builders never wait for a slot; with one piece per CTA (384 threads) warps 8-11 write it
+    // after building.
+    const bool dedicated_writers = blockDim.x > 384;
+    if (dedicated_writers ? warp >= 12 : (warp >= 8 && warp < 12)) {
         const int q4 = warp & 3;
         const int r = q4 * 32 + lane;
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
         constexpr int LAST_ROW = CF::ZROW ? V : V - 1;
-        float *slot = slots + static_cast<size_t>(blockIdx.x) * CF::SLOT;
-        if (wait_bar(BAR(AB_AGG_DONE), 0, abort_flag, SITE_AGG_DONE)) {
+        for (int kk = 0; kk < p1 - p0; ++kk) {
+            const int b = kk & 1;
+            if (!wait_bar(BAR(AB_AGG_DONE0 + b), (kk >> 1) & 1, abort_flag, SITE_AGG_DONE)) break;
             tc_fence_after();
-            if (warp == 8 && lane == 0) BASED_TRACE_EV(40, 5);
+            if (q4 == 0 && lane == 0) BASED_TRACE_EV(40, 5);
+            float *slot = slots + static_cast<size_t>(p0 + kk) * CF::SLOT;
+            const uint32_t acc = tmem + lo + b * kAggAccStride;
             if (q4 * 32 <= LAST_ROW) {
-                // two feature blocks per TMEM round trip; element (c, r) at c * SROWS + r
+                // two feature blocks per TMEM round trip
 #pragma unroll 1
                 for (int f = 0; f < CF::NBLK; f += 2) {
                     uint32_t x[2][16];
-                    tmem_ld_x16(tmem + lo + 16 * f, x[0]);
-                    if (f + 1 < CF::NBLK) tmem_ld_x16(tmem + lo + 16 * (f + 1), x[1]);
+                    tmem_ld_x16(acc + 16 * f, x[0]);
+                    if (f + 1 < CF::NBLK) tmem_ld_x16(acc + 16 * (f + 1), x[1]);
                     tmem_wait_ld_dep(x[0]);
                     tmem_wait_ld_dep(x[1]);
                     if (r <= LAST_ROW) {
@@ -1321,61 +1529,38 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             }
             if constexpr (!CF::ZROW) {
                 uint32_t za, zb;
-                tmem_ld_x1(tmem + lo + CF::TA_Z, za);
-                tmem_ld_x1(tmem + lo + CF::TA_Z + 16, zb);
+                tmem_ld_x1(acc + CF::TA_Z, za);
+                tmem_ld_x1(acc + CF::TA_Z + 16, zb);
                 tmem_wait_ld();
                 float *zcol = slot + V;  // element (c, V) at c * SROWS + V
                 if (r < CF::PP && r < 128) zcol[static_cast<size_t>(r) * CF::SROWS] = __uint_as_float(za);
                 if (r + 32 >= 128 && r + 32 < CF::PP)
                     zcol[static_cast<size_t>(r + 32) * CF::SROWS] = __uint_as_float(zb);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(AB_SLOT_READ0 + b));  // the accumulator may be reused
         }
     }
 
-    if (warp == 8 && lane == 0) BASED_TRACE_EV(40, 6);
 #ifdef BASED_TRACE
-    if (warp == 8 && lane == 0 && trace_buf_ != nullptr)
+    if (threadIdx.x == 0 && trace_buf_ != nullptr)
         trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 40) * 32 + 9] = global_timer_ns();
 #endif
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, tmem_cols);
     }
 }
+
 
 // ------------------------------------------------------------------------------------------------
 // Scan: within each run of ranges that continue one head's prefix, turn the per-range partial
 // states into inclusive prefixes (slot i = sum of the partial states of ranges <= i in the run).
 // The runs are listed by the host: block (x, r) handles a slice of the elements of run r.
 // ------------------------------------------------------------------------------------------------
-constexpr int kMaxRanges = 256;  // upper bound on G (one range per SM)
-struct ScanRuns {
-    int n;                         // number of runs with more than one range
-    uint16_t start[kMaxRanges];    // first slot of the run
-    uint16_t len[kMaxRanges];      // slots in the run (>= 2)
-};
-
-// Lists the runs of G ranges whose partial states chain into one head's prefix: a run starts at a
-// range with an aggregate that does not continue a prefix and extends over the ranges that do.
-// Single-range runs need no scan and are left out.
-inline ScanRuns make_scan_runs(long long N, int G, int n_c) {
-    ScanRuns runs;
-    runs.n = 0;
-    for (int i = 0; i < G; ++i) {
-        if (!has_aggregate(N, G, i, n_c) || continues_prefix(N, G, i, n_c)) continue;
-        int j = i + 1;
-        while (j < G && continues_prefix(N, G, j, n_c) && has_aggregate(N, G, j, n_c)) ++j;
-        if (j - i >= 2) {
-            runs.start[runs.n] = static_cast<uint16_t>(i);
-            runs.len[runs.n] = static_cast<uint16_t>(j - i);
-            ++runs.n;
-        }
-    }
-    return runs;
-}
-
 __global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems,
                                   const __grid_constant__ ScanRuns runs) {
     griddep_launch_dependents();
