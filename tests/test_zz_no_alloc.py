@@ -1,11 +1,11 @@
 """The allocation-free entry point (based_fwd_noalloc, scratch in a fixed device array) against
 the regular entry point (based_fwd, library-owned workspace), both called through the C ABI.
 
-Two calls in a row with different shapes and inputs: the second must not see anything the first
-left in the shared scratch array. Both shapes split heads across CTAs, so the aggregate and scan
-kernels run and the scratch is used. Tolerance: the parity bar of the GPU tests (max |diff| <=
-2e-2, mean |diff| <= 2e-3); the two entry points launch the same kernels, so in practice they agree
-exactly.
+Calls in a row with different shapes and inputs: a later one must not see anything an earlier one
+left in the shared scratch array. Every shape splits heads across CTAs, so the aggregate kernel
+(and the scan, where the plan needs it) runs and the scratch is used. Tolerance: the parity bar of
+the GPU tests (max |diff| <= 2e-2, mean |diff| <= 2e-3); where both entry points use the same
+plan they agree exactly, and the last shape checks the smaller plan the scratch forces.
 """
 import ctypes
 
@@ -21,6 +21,10 @@ MAX_ABS, MEAN_ABS = 2e-2, 2e-3
 SHAPES = [  # B, T, H, K, V, seed
     (2, 2048, 8, 16, 64, 41),
     (1, 3000, 6, 8, 128, 42),
+    # based_fwd cuts this shape's aggregate pass into 288 pieces (one slot each), which would not
+    # fit the 16 MiB scratch at 82,560 bytes per slot: the no-allocation call keeps one slot per
+    # range and sums in another order
+    (2, 16384, 32, 16, 128, 43),
 ]
 
 
@@ -38,7 +42,7 @@ def test_noalloc_matches_based_fwd_twice(cuda_device):
     L = library()
     device_status(0, clear=True)
     for B, T, H, K, V, seed in SHAPES:
-        assert workspace_size(B, T, H, K, V) > 0 and kernel_count(B, T, H, K, V) == 3
+        assert workspace_size(B, T, H, K, V) > 0 and kernel_count(B, T, H, K, V) >= 2
         q, k, v = (x.to(cuda_device) for x in make_inputs(B, T, H, K, V, seed))
         o_ref = torch.empty(B, T, H, V, dtype=torch.float32, device=cuda_device)
         o_na = torch.full_like(o_ref, float("nan"))
