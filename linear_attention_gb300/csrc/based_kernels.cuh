@@ -1291,27 +1291,31 @@ struct AggBar {
 };
 constexpr uint32_t kAggAccStride = 256;  // TMEM columns between the two accumulators
 
-// Walks the chunks of pieces p .. p_end - 1 in order.
+// Walks the chunks of pieces p .. p_end - 1 in order (the piece table is read once per piece).
 struct PieceWalk {
     Cursor cu;
     const AggPieces *ap;
-    int p, p_end, j, n_c, H;
+    int p, p_end, j, len, n_c, H;
+    __device__ __forceinline__ void start_piece() {
+        len = ap->len[p];
+        cu.init(ap->g0[p], len, n_c, H);
+    }
     __device__ __forceinline__ void init(const AggPieces &a, int p0, int p1, int n_c_, int H_) {
         ap = &a;
         p = p0;
         p_end = p1;
         j = 0;
+        len = 0;
         n_c = n_c_;
         H = H_;
-        if (p < p_end) cu.init(a.g0[p], a.len[p], n_c, H);
+        if (p < p_end) start_piece();
     }
-    __device__ __forceinline__ bool done() const { return p >= p_end; }
     __device__ __forceinline__ bool first() const { return j == 0; }
-    __device__ __forceinline__ bool last() const { return j == ap->len[p] - 1; }
+    __device__ __forceinline__ bool last() const { return j == len - 1; }
     __device__ __forceinline__ void next() {
-        if (++j == ap->len[p]) {
+        if (++j == len) {
             j = 0;
-            if (++p < p_end) cu.init(ap->g0[p], ap->len[p], n_c, H);
+            if (++p < p_end) start_piece();
         } else {
             cu.next();
         }
