@@ -51,9 +51,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // (dim0, H, T, B) tensor of 2-byte (bf16) or 4-byte (fp32) elements with a
-// (box0, 1, box_rows, 1) box.
+// (box0, 1, box_rows, 1) box. promo: how far L2 widens a miss of the box's rows.
 int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, int box0,
-             CUtensorMapSwizzle swz, bool fp32 = false, int box_rows = kChunk) {
+             CUtensorMapSwizzle swz, CUtensorMapL2promotion promo, bool fp32 = false,
+             int box_rows = kChunk) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) {
         snprintf(tl_cuda_error, sizeof(tl_cuda_error), "cuTensorMapEncodeTiled unavailable");
@@ -70,7 +71,7 @@ int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, in
     CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                      const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         snprintf(tl_cuda_error, sizeof(tl_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
                  static_cast<int>(r));
@@ -208,12 +209,20 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     CUtensorMap mq, mk, mv, mo;
     int rc;
     const CUtensorMapSwizzle sw_qk = CU_TENSOR_MAP_SWIZZLE_32B;
-    if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
-    if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk)) != BASED_OK) return rc;
-    if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != BASED_OK) return rc;
-    // output boxes of 128-byte rows: 32 fp32 or 64 bf16 columns
-    if ((rc = make_map(&mo, o, V, B, T, H, OBF ? 64 : 32, CU_TENSOR_MAP_SWIZZLE_128B, !OBF, CF::EPI_ROWS)) !=
+    // A q or k row of one head is 16 or 32 bytes, 1/8 or 1/4 of a 128-byte line whose other bytes
+    // are other heads' rows, read by other CTAs at other times (on inputs much larger than L2,
+    // after the line has left it). Their misses are widened to 64 bytes, not to the 128 of the
+    // v and o rows (whole lines): on B=8 T=16384 H=32 K=8 V=128 that cuts the forward kernel
+    // from 700 to 637 us (no promotion measures like 128 bytes).
+    const CUtensorMapL2promotion promo_qk = CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
+    if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk, promo_qk)) != BASED_OK) return rc;
+    if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk, promo_qk)) != BASED_OK) return rc;
+    if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) !=
         BASED_OK)
+        return rc;
+    // output boxes of 128-byte rows: 32 fp32 or 64 bf16 columns
+    if ((rc = make_map(&mo, o, V, B, T, H, OBF ? 64 : 32, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, !OBF, CF::EPI_ROWS)) != BASED_OK)
         return rc;
     if (p.need_agg) {
         // 512 threads (dedicated slot writers) when a CTA sums several pieces, else 384
