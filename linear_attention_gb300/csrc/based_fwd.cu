@@ -82,8 +82,9 @@ int make_map(CUtensorMap *map, const void *base, int d0, int B, int T, int H, in
 
 struct Plan {
     int n_c;        // chunks per head
-    long long N;    // chunks in total
-    int G;          // CTAs
+    int L;          // head lanes (choose_lanes); every lane has the same partition and plan
+    long long N;    // chunks of one lane
+    int G;          // ranges of one lane (forward CTAs: G L)
     bool need_agg;  // some range ends inside a head
     int slot_floats;
     size_t ws_bytes;
@@ -136,17 +137,19 @@ int slot_floats(int K, int V) { return (V + 1) * ((K == 16) ? 160 : 48); }
 Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~static_cast<size_t>(0)) {
     Plan p;
     p.n_c = (T + kChunk - 1) / kChunk;
-    p.N = static_cast<long long>(B) * H * p.n_c;
-    const int gmax = sms < kMaxRanges ? sms : kMaxRanges;
+    const long long n_all = static_cast<long long>(B) * H * p.n_c;
+    p.L = choose_lanes(K, H, n_all, sms);
+    p.N = n_all / p.L;
+    const int gmax = sms / p.L < kMaxRanges ? sms / p.L : kMaxRanges;
     p.G = static_cast<int>(p.N < gmax ? p.N : gmax);
     p.need_agg = false;
     for (int i = 0; i < p.G; ++i)
         if (has_aggregate(p.N, p.G, i, p.n_c)) p.need_agg = true;
     p.slot_floats = slot_floats(K, V);
     const size_t slot_bytes = static_cast<size_t>(p.slot_floats) * sizeof(float);
-    const size_t max_slots = max_ws / slot_bytes;
+    const size_t max_slots = max_ws / slot_bytes / p.L;  // per lane
     make_agg_plan(p.N, p.G, p.n_c, p.G, max_slots < kMaxPieces ? static_cast<int>(max_slots) : kMaxPieces, p.agg);
-    p.ws_bytes = p.need_agg ? static_cast<size_t>(p.agg.pieces.n) * slot_bytes : 0;
+    p.ws_bytes = p.need_agg ? static_cast<size_t>(p.L) * p.agg.pieces.n * slot_bytes : 0;
     return p;
 }
 
@@ -209,12 +212,13 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     CUtensorMap mq, mk, mv, mo;
     int rc;
     const CUtensorMapSwizzle sw_qk = CU_TENSOR_MAP_SWIZZLE_32B;
-    // A q or k row of one head is 16 or 32 bytes, 1/8 or 1/4 of a 128-byte line whose other bytes
-    // are other heads' rows, read by other CTAs at other times (on inputs much larger than L2,
-    // after the line has left it). Their misses are widened to 64 bytes, not to the 128 of the
-    // v and o rows (whole lines): on B=8 T=16384 H=32 K=8 V=128 that cuts the forward kernel
-    // from 700 to 637 us (no promotion measures like 128 bytes).
-    const CUtensorMapL2promotion promo_qk = CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
+    // A q or k row of one head is 16 or 32 bytes of a 128-byte line shared with adjacent heads.
+    // A miss fetches 64 bytes, or the whole line when four head lanes of 32-byte rows (K = 16)
+    // read all of it at about the same time. Without lanes the rest of a longer fetch would be
+    // read by other CTAs long after it left L2 (on inputs much larger than L2); with eight lanes
+    // of 16-byte rows (K = 8) 64 bytes measure about 1 % faster. No promotion measures like 128.
+    const CUtensorMapL2promotion promo_qk =
+        (K == 16 && p.L == 4) ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
     if ((rc = make_map(&mq, q, K, B, T, H, 16, sw_qk, promo_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mk, k, K, B, T, H, 16, sw_qk, promo_qk)) != BASED_OK) return rc;
     if ((rc = make_map(&mv, v, V, B, T, H, 64, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) !=
@@ -227,13 +231,13 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     if (p.need_agg) {
         // 512 threads (dedicated slot writers) when a CTA sums several pieces, else 384
         const int threads = p.agg.pieces.n > p.agg.pieces.n_cta ? kAggThreads : 384;
-        based_agg_kernel<K, V><<<p.agg.pieces.n_cta, threads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c,
-                                                                              p.agg.pieces);
+        based_agg_kernel<K, V><<<p.agg.pieces.n_cta * p.L, threads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.L,
+                                                                                    p.agg.pieces);
         BASED_CUDA(cudaGetLastError());
         if (p.agg.scan) {  // otherwise each forward CTA sums the (at most kMaxChain) slots it needs
-            dim3 grid((p.slot_floats / 4 + 255) / 256, p.agg.runs.n);
+            dim3 grid((p.slot_floats / 4 + 255) / 256, p.agg.runs.n * p.L);
             BASED_CUDA(launch_dependent(based_scan_kernel, grid, dim3(256), 0, st, true, ws,
-                                        p.slot_floats, p.agg.runs));
+                                        p.slot_floats, p.agg.pieces.n, p.agg.runs));
         }
     }
     if (ev_begin) BASED_CUDA(cudaEventRecord(ev_begin, st));
@@ -242,9 +246,9 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     // aggregate pass, or when the caller brackets it with events, it is an ordinary launch: it
     // must not start before earlier work in the stream that may produce q, k or v.
     const bool dependent = p.need_agg && !ev_begin;
-    BASED_CUDA(launch_dependent(based_fwd_kernel<K, V, OBF>, dim3(p.G), dim3(kFwdThreads), CF::SMEM_FWD, st,
+    BASED_CUDA(launch_dependent(based_fwd_kernel<K, V, OBF>, dim3(p.G * p.L), dim3(kFwdThreads), CF::SMEM_FWD, st,
                                 dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
-                                p.N, p.G, scale, p.agg.pre));
+                                p.N, p.G, p.L, p.agg.pieces.n, scale, p.agg.pre));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }
@@ -398,8 +402,15 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     const size_t bq = up(rows * K * 2), bv = up(rows * V * 2), bo = up(rows * V * 4);
     const size_t need = 2 * bq + bv + bo;
-    // workspace of the largest piece (pieces run one after another on the compute stream)
-    const size_t ws_piece = up(make_plan((B + nb - 1) / nb, T, (H + nh - 1) / nh, K, V, d.sms).ws_bytes);
+    // the most workspace any piece needs (pieces run one after another on the compute stream; a
+    // piece has B / nb or B / nb + 1 batch entries and H / nh or H / nh + 1 heads)
+    size_t ws_piece = 0;
+    for (int pb : {B / nb, (B + nb - 1) / nb})
+        for (int hp : {H / nh, (H + nh - 1) / nh})
+            if (pb > 0 && hp > 0) {
+                const size_t w = up(make_plan(pb, T, hp, K, V, d.sms).ws_bytes);
+                ws_piece = w > ws_piece ? w : ws_piece;
+            }
     uint8_t *base, *wsb;
     {
         std::lock_guard<std::mutex> lk(d.m);

@@ -322,8 +322,19 @@ constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
 constexpr uint32_t kBf16Half2 = 0x3F003F00u;  // bf16 pair (0.5, 0.5)
 
 // ------------------------------------------------------------------------------------------------
-// Work partition: the B*H*n_c chunks, ordered head-major, are cut into G contiguous ranges.
+// Work partition. The heads are dealt into L lanes (lane r: heads h = r, r + L, ...), and each
+// lane's B*(H/L)*n_c chunks, ordered head-major, are cut into G contiguous ranges, the same cut
+// in every lane. CTA j L + r takes range j of lane r. The L CTAs of a group then work on the same
+// positions of L adjacent heads at the same time, and the q/k rows of those heads, which share
+// 128-byte lines, are read from DRAM once instead of once per head.
 // ------------------------------------------------------------------------------------------------
+// Lanes: as many as adjacent heads' q/k rows fill a 128-byte line (4 for K = 16, 8 for K = 8),
+// halved until they divide H and the CTA count (sms CTAs over N chunks) splits evenly over them.
+__host__ __device__ inline int choose_lanes(int K, int H, long long N, int sms) {
+    int L = 128 / (2 * K);
+    while (L > 1 && (H % L != 0 || (N > sms && sms % L != 0) || sms < L)) L /= 2;
+    return L;
+}
 struct Part {
     long long g0, g1;
 };
@@ -501,26 +512,32 @@ inline void make_agg_plan(long long N, int G, int n_c, int max_cta, int max_slot
 }
 
 // Walks the chunks of a range without divisions: (b, h, c) advance like an odometer.
+// g is a chunk index of one head lane (see choose_lanes): lane r's heads are h = hv L + r,
+// hv < Hl = H / L.
 struct Cursor {
-    int n, last, c, h, b, n_c, H;
-    __device__ __forceinline__ void init(long long g, int nchunks, int n_c_, int H_) {
+    int n, last, c, hv, h, b, n_c, Hl, L, r;
+    __host__ __device__ __forceinline__ void init(long long g, int nchunks, int n_c_, int Hl_, int L_, int r_) {
         n_c = n_c_;
-        H = H_;
+        Hl = Hl_;
+        L = L_;
+        r = r_;
         n = 0;
         last = nchunks - 1;
         const long long head = g / n_c;
         c = static_cast<int>(g - head * n_c);
-        h = static_cast<int>(head % H);
-        b = static_cast<int>(head / H);
+        hv = static_cast<int>(head % Hl);
+        b = static_cast<int>(head / Hl);
+        h = hv * L + r;
     }
-    __device__ __forceinline__ void next() {
+    __host__ __device__ __forceinline__ void next() {
         ++n;
         if (++c == n_c) {
             c = 0;
-            if (++h == H) {
-                h = 0;
+            if (++hv == Hl) {
+                hv = 0;
                 ++b;
             }
+            h = hv * L + r;
         }
     }
     __device__ __forceinline__ int t0() const { return c * kChunk; }
@@ -551,8 +568,8 @@ template <int K, int V, bool OBF>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G,
-                 float scale, const __grid_constant__ Prefixes pre) {
+                 const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G, int L,
+                 int lane_slots, float scale, const __grid_constant__ Prefixes pre) {
     using CF = Cfg<K, V>;
     constexpr bool FAST = CF::FAST;
     extern __shared__ uint8_t smem_raw[];
@@ -570,7 +587,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto sbf_full_bar = [&](int k) -> int { return (CF::NSBF == 2 && (k & 1)) ? FB_SBF_FULL1 : FB_SBF_FULL; };
     auto sbf_full_par = [&](int k) -> uint32_t { return static_cast<uint32_t>(CF::NSBF == 2 ? (k >> 1) & 1 : k & 1); };
 
-    const Part part = cta_range(N, G, blockIdx.x);
+    // range j of head lane r (N, G: chunks and ranges of one lane; lane_slots: slots per lane)
+    const int j_range = static_cast<int>(blockIdx.x) / L, r_lane = static_cast<int>(blockIdx.x) % L;
+    const int Hl = H / L;
+    const Part part = cta_range(N, G, j_range);
     const long long g0 = part.g0, g1 = part.g1;
     const int nchunks = static_cast<int>(g1 - g0);
     if (nchunks <= 0) return;
@@ -612,7 +632,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_o);
         Cursor cu;
-        cu.init(g0, nchunks, n_c, H);
+        cu.init(g0, nchunks, n_c, Hl, L, r_lane);
         for (int n = 0; n < n_early; ++n, cu.next()) issue_loads(n, cu);
     }
     // bf16 state operands: zero once (rows V+2.. stay zero; rows 0..V+1 are rewritten per use).
@@ -649,7 +669,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             int issued = n_early;
             Cursor cu;
-            cu.init(g0, nchunks, n_c, H);
+            cu.init(g0, nchunks, n_c, Hl, L, r_lane);
             for (int n = 0; n < n_early; ++n) cu.next();
             for (int n = n_early; n < nchunks; ++n, cu.next()) {
                 const int s = n % CF::NST;
@@ -688,7 +708,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint64_t d_va0 = va_desc(0), d_va1 = va_desc(1), d_va2 = va_desc(CF::NST > 2 ? 2 : 1);
             const uint64_t d_zones = smem_desc(sb + CF::OFF_ZONES, 16, 256, LAYOUT_SW32);
             Cursor cu;
-            cu.init(g0, nchunks, n_c, H);
+            cu.init(g0, nchunks, n_c, Hl, L, r_lane);
             if (warp == 1) {
                 // ---- intra-chunk stream: QK(0); per chunk QK(n + 1) and AV(n) ----
                 constexpr uint32_t ID_QK = idesc_bf16_f32(128, 128, 0, 0);
@@ -1060,7 +1080,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             return true;
         };
         Cursor cu;
-        cu.init(g0, nchunks, n_c, H);
+        cu.init(g0, nchunks, n_c, Hl, L, r_lane);
         int pb = 0, ph = 0, pt0 = 0;  // coordinates of the previous chunk (for its epilogue)
         for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
             const int s = n % CF::NST;
@@ -1187,11 +1207,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         int cidx = 0;
         // A range that starts inside a head continues from the prefix state of the chunks before
         // it: load it into TMEM, then convert it like any other state.
-        if (pre.cnt[blockIdx.x] > 0) {
+        if (pre.cnt[j_range] > 0) {
             // The prefix is the sum of the partial states of the pieces of the head before this
             // range: slots pre.slot .. pre.slot + m - 1 (m <= kMaxChain; m = 1 when a scan has
             // already summed them).
-            const int m = pre.cnt[blockIdx.x];
+            const int m = pre.cnt[j_range];
             // launched as a dependent of the aggregate / scan kernel: only this read of their
             // output waits for them (every other role starts right away)
             griddep_wait();
@@ -1199,7 +1219,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (r == 0 && trace_buf_ != nullptr)
                 trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 24] = global_timer_ns();
 #endif
-            const float *slot = prefix + static_cast<size_t>(pre.slot[blockIdx.x]) * CF::SLOT;
+            const float *slot =
+                prefix + (static_cast<size_t>(pre.slot[j_range]) + static_cast<size_t>(r_lane) * lane_slots) * CF::SLOT;
             // One code path per chain length, so that every load it issues is needed and all of a
             // step's loads are in flight together; the terms are summed in range order.
             auto load_prefix = [&](auto chain_len) {
@@ -1247,7 +1268,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         int u = 0;
         Cursor cu;
-        cu.init(g0, nchunks, n_c, H);
+        cu.init(g0, nchunks, n_c, Hl, L, r_lane);
         for (int n = 0; n < nchunks; ++n, cu.next()) {
             if (!cu.has_upd()) continue;
             if (!wait_bar(BAR(FB_UPD_DONE), u & 1, abort_flag, SITE_UPD_DONE)) break;
@@ -1295,19 +1316,21 @@ constexpr uint32_t kAggAccStride = 256;  // TMEM columns between the two accumul
 struct PieceWalk {
     Cursor cu;
     const AggPieces *ap;
-    int p, p_end, j, len, n_c, H;
+    int p, p_end, j, len, n_c, Hl, L, r;
     __device__ __forceinline__ void start_piece() {
         len = ap->len[p];
-        cu.init(ap->g0[p], len, n_c, H);
+        cu.init(ap->g0[p], len, n_c, Hl, L, r);
     }
-    __device__ __forceinline__ void init(const AggPieces &a, int p0, int p1, int n_c_, int H_) {
+    __device__ __forceinline__ void init(const AggPieces &a, int p0, int p1, int n_c_, int Hl_, int L_, int r_) {
         ap = &a;
         p = p0;
         p_end = p1;
         j = 0;
         len = 0;
         n_c = n_c_;
-        H = H_;
+        Hl = Hl_;
+        L = L_;
+        r = r_;
         if (p < p_end) start_piece();
     }
     __device__ __forceinline__ bool first() const { return j == 0; }
@@ -1325,7 +1348,7 @@ struct PieceWalk {
 template <int K, int V>
 __global__ void __launch_bounds__(kAggThreads, 1)
 based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 float *__restrict__ slots, int H, int n_c, const __grid_constant__ AggPieces ap) {
+                 float *__restrict__ slots, int H, int n_c, int L, const __grid_constant__ AggPieces ap) {
     using CF = Cfg<K, V>;
     constexpr int S = CF::A_NST;
     constexpr int NP = CF::A_NPHIK;
@@ -1337,8 +1360,12 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                   AB_PHIK_FULL0 = AB::PHIK_FULL0, AB_PHIK_FREE0 = AB::PHIK_FREE0,
                   AB_AGG_DONE0 = AB::AGG_DONE0, AB_SLOT_READ0 = AB::SLOT_READ0, AB_DRAIN = AB::DRAIN,
                   AB_COUNT = AB::COUNT;
-    if (static_cast<int>(blockIdx.x) >= ap.n_cta) return;
-    const int p0 = ap.cta_first[blockIdx.x], p1 = ap.cta_first[blockIdx.x + 1];
+    // CTA a L + r sums CTA a's pieces of head lane r into that lane's slots
+    const int a_cta = static_cast<int>(blockIdx.x) / L, r_lane = static_cast<int>(blockIdx.x) % L;
+    const int Hl = H / L;
+    if (a_cta >= ap.n_cta) return;
+    slots += static_cast<size_t>(r_lane) * ap.n * CF::SLOT;
+    const int p0 = ap.cta_first[a_cta], p1 = ap.cta_first[a_cta + 1];
     int nchunks = 0;
     for (int p = p0; p < p1; ++p) nchunks += ap.len[p];
     if (nchunks <= 0) return;
@@ -1381,7 +1408,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         PieceWalk w;
-        w.init(ap, p0, p1, n_c, H);
+        w.init(ap, p0, p1, n_c, Hl, L, r_lane);
         for (int u = 0; u < n_early; ++u, w.next()) issue_loads(u, w.cu);
     }
     if constexpr (CF::ZROW) {
@@ -1411,7 +1438,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         if (lane == 0) {
             int issued = n_early;
             PieceWalk w;
-            w.init(ap, p0, p1, n_c, H);
+            w.init(ap, p0, p1, n_c, Hl, L, r_lane);
             for (int u = 0; u < n_early; ++u) w.next();
             for (int u = n_early; u < nchunks; ++u, w.next()) {
                 const int s = u % S;
@@ -1433,7 +1460,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
             const uint64_t d_zones = smem_desc(sb + CF::A_OFF_ZONES, 16, 256, LAYOUT_SW32);
             PieceWalk w;
-            w.init(ap, p0, p1, n_c, H);
+            w.init(ap, p0, p1, n_c, Hl, L, r_lane);
             int kk = 0;  // pieces of this CTA started
             for (int u = 0; u < nchunks; ++u, w.next()) {
                 const int s = u % S, pb = u % NP, b = kk & 1;
@@ -1563,15 +1590,17 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 // ------------------------------------------------------------------------------------------------
 // Scan: within each run of ranges that continue one head's prefix, turn the per-range partial
 // states into inclusive prefixes (slot i = sum of the partial states of ranges <= i in the run).
-// The runs are listed by the host: block (x, r) handles a slice of the elements of run r.
+// The runs are listed by the host: block (x, l runs.n + r) handles a slice of the elements of run r
+// of head lane l.
 // ------------------------------------------------------------------------------------------------
-__global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems,
+__global__ void based_scan_kernel(float *__restrict__ slots, int slot_elems, int lane_slots,
                                   const __grid_constant__ ScanRuns runs) {
     griddep_launch_dependents();
     griddep_wait();  // the aggregate kernel's slots are complete and visible
-    const int r = blockIdx.y;
-    if (r >= runs.n) return;
-    const int i0 = runs.start[r], len = runs.len[r];
+    if (runs.n == 0) return;
+    // blockIdx.y = lane * runs.n + run (every head lane has the same runs)
+    const int r = static_cast<int>(blockIdx.y) % runs.n, lane = static_cast<int>(blockIdx.y) / runs.n;
+    const int i0 = runs.start[r] + lane * lane_slots, len = runs.len[r];
     const int vec = slot_elems / 4;  // slots are whole float4s
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < vec; e += gridDim.x * blockDim.x) {
         float4 *p = reinterpret_cast<float4 *>(slots + static_cast<size_t>(i0) * slot_elems) + e;
