@@ -155,9 +155,9 @@ BASED_API int based_fwd_timed(const uint16_t *q, const uint16_t *k, const uint16
                               void *ev_begin, void *ev_end);
 
 /* Number of kernels one based_fwd call launches for this shape on the current device: 1 (the
- * forward kernel alone), 2 (aggregate, forward: every prefix is the sum of at most two partial
- * states, which the forward kernel adds itself) or 3 (aggregate, scan, forward: some head spans
- * more than three ranges); 0 for an unsupported shape. */
+ * forward kernel alone), 2 (aggregate, forward: every prefix is the sum of at most four partial
+ * states, which the forward kernel adds itself) or 3 (aggregate, scan, forward: some prefix has
+ * more); 0 for an unsupported shape. */
 BASED_API int based_fwd_kernel_count(int B, int T, int H, int K, int V);
 
 /* Reads (and, if clear != 0, resets) the device status word of `device`: 0 means no kernel of

@@ -24,7 +24,7 @@
 namespace based {
 
 constexpr int kChunk = 128;            // rows per chunk = MMA M
-constexpr int kMaxChain = 2;           // partial states a forward CTA sums into its prefix itself
+constexpr int kMaxChain = 4;           // partial states a forward CTA sums into its prefix itself
 constexpr int kFwdThreads = 512;       // 4 warpgroups
 constexpr int kAggThreads = 512;       // 4 warpgroups
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after 1 s
@@ -61,7 +61,7 @@ enum TraceEvent {
 enum WaitSite : uint32_t {
     SITE_STAGE_FREE = 1, SITE_TMA_FULL, SITE_S_FULL, SITE_A_FULL, SITE_O_FULL, SITE_O_FREE,
     SITE_AV_DONE, SITE_PHIQ_FULL, SITE_PHIQ_FREE, SITE_PHIK_FULL, SITE_PHIK_FREE, SITE_UPD_DONE,
-    SITE_SBF_FULL, SITE_CONV_READ, SITE_AGG_DONE, SITE_DRAIN, SITE_SLOT_READ, SITE_SELFTEST = 255
+    SITE_SBF_FULL, SITE_CONV_READ, SITE_AGG_DONE, SITE_DRAIN, SITE_SLOT_READ, SITE_ZRED, SITE_SELFTEST = 255
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t site) {
@@ -139,9 +139,6 @@ struct Cfg {
     static constexpr int TM_O1 = FAST ? TM_O0 + NO : TM_O0;
     static constexpr int TM_Z = align_up(TM_O1 + NO, 32);           // z tiles (V = 128)
     static_assert(ZROW ? (TM_O1 + NO <= 512) : (TM_Z + 32 <= 512), "TMEM overflow");
-    // TMEM columns (aggregate kernel)
-    static constexpr int TA_Z = align_up(PP, 32);
-    static_assert(TA_Z + 32 <= 256, "TMEM overflow (aggregate)");
 
     // Shared memory (forward kernel), byte offsets from a 1024-aligned base.
     static constexpr int RAW = kChunk * 32;    // one raw q or k tile: 128 rows x 16 bf16
@@ -179,21 +176,28 @@ struct Cfg {
     static_assert(ZROW || OFF_PHIK + 8 * 4096 <= OFF_BAR, "z MMA window leaves shared memory");
     static_assert(SMEM_FWD <= 232448, "shared memory budget");
 
-    // Shared memory (aggregate kernel): A_NPHIK phi(k) buffers and as many k/v stages as fit (at
-    // most 8), so that the loads run far enough ahead to hide the memory latency.
-    // three f(k) buffers where they leave room for 4+ stages (the builders then run two chunks
-    // ahead of the state update), else two
-    static constexpr int A_NPHIK = (232448 - 4352 - align_up(3 * PHI, 1024)) / (RAW + VT) >= 4 ? 3 : 2;
-    static constexpr int A_NST_FIT = (232448 - 1024 - 256 - 1024 - 2048 - align_up(A_NPHIK * PHI, 1024)) / (RAW + VT);
+    // Shared memory (aggregate kernel): A_NPHIK f(k) buffers and as many k/v stages as fit (at
+    // most 8), so that the loads run far enough ahead to hide the memory latency. Three f(k)
+    // buffers where they leave room for 4+ stages (the builders then run two chunks ahead of the
+    // state update); for K = 16, V = 128 one, since a second would cost the fifth stage and the
+    // state update (no z MMAs) is short next to the memory latency; else two.
+    // V = 128: per-warp partial sums of z (two buffers, used by alternate pieces, of 8 builder
+    // warps x half a feature row, fp32)
+    static constexpr int A_ZRED = ZROW ? 0 : 2 * 8 * ((NBLK + 1) / 2) * 16 * 4;
+    static constexpr int A_NPHIK = (!ZROW && K == 16) ? 1
+                                   : (232448 - 4352 - align_up(3 * PHI, 1024)) / (RAW + VT) >= 4 ? 3 : 2;
+    // (alignment slack, barriers, z partial sums, ones block)
+    static constexpr int A_NST_FIT =
+        (232448 - 1024 - 256 - A_ZRED - ONES - align_up(A_NPHIK * PHI, 1024)) / (RAW + VT);
     static constexpr int A_NST = A_NST_FIT < 8 ? A_NST_FIT : 8;
     static constexpr int A_OFF_PHIK = 0;
     static constexpr int A_OFF_RAWK = align_up(A_NPHIK * PHI, 1024);
     static constexpr int A_OFF_V = A_OFF_RAWK + A_NST * RAW;
     static constexpr int A_OFF_ONES = A_OFF_V + A_NST * VT;
-    static constexpr int A_OFF_ZONES = align_up(A_OFF_ONES + ONES, 1024);
-    static constexpr int A_OFF_BAR = A_OFF_ZONES + 1024;
-    static constexpr int SMEM_AGG = A_OFF_BAR + 256 + 1024;
-    static_assert(ZROW || A_OFF_PHIK + (A_NPHIK - 1) * PHI + 8 * 4096 <= A_OFF_BAR, "z MMA window (aggregate)");
+    static constexpr int A_OFF_BAR = A_OFF_ONES + ONES;
+    static constexpr int A_OFF_ZRED = A_OFF_BAR + 256;
+    static constexpr int SMEM_AGG = A_OFF_ZRED + A_ZRED + 1024;
+    static_assert(8 * (2 * A_NST + 2 * A_NPHIK + 6) + 8 <= A_OFF_ZRED - A_OFF_BAR, "barriers (aggregate)");
     static_assert(SMEM_AGG <= 232448, "shared memory budget (aggregate)");
 };
 
@@ -257,6 +261,8 @@ __device__ __forceinline__ uint32_t taylor2(uint32_t s_lo, uint32_t s_hi, uint64
 // Only blocks f_lo <= f < f_hi are built (two threads can share a token row).
 // Out of line: the q and k builders share one copy of the code, which keeps the kernel's
 // instruction-cache footprint small.
+constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
+constexpr uint32_t kBf16Half2 = 0x3F003F00u;  // bf16 pair (0.5, 0.5)
 template <int K>
 __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t sig2,
                                             uint32_t half2, int f_lo, int f_hi) {
@@ -318,8 +324,125 @@ __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, u
                       bmul2(X[0], X[2]), bmul2(X[1], X[3]), ONE_ZERO, 0u);
     }
 }
-constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
-constexpr uint32_t kBf16Half2 = 0x3F003F00u;  // bf16 pair (0.5, 0.5)
+
+// f(k) of token t for feature blocks [F0, F1) (half of the row, fixed at compile time), stored as
+// build_features stores it (the same products, bit for bit), with every feature also added to
+// z[16 (f - F0) + j] (fp32; feature j of block f), so that the aggregate pass gets z = sum f(k)
+// without an MMA.
+template <int K, int F0, int F1>
+__device__ __forceinline__ void build_k_features_acc(uint32_t raw, uint32_t phi, int t, float (&z)[(F1 - F0) * 16]) {
+    const uint32_t rb = raw + static_cast<uint32_t>(t) * 32u;
+    const uint32_t sw = static_cast<uint32_t>(((t >> 2) & 1) << 4);
+    auto put = [&](int f, const uint32_t (&w)[8]) {
+        const uint32_t base = phi + static_cast<uint32_t>(f) * 4096u + static_cast<uint32_t>(t) * 32u;
+        st_shared_v4(base + sw, w[0], w[1], w[2], w[3]);
+        st_shared_v4(base + (16u ^ sw), w[4], w[5], w[6], w[7]);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            z[16 * (f - F0) + 2 * m] += __uint_as_float(w[m] << 16);
+            z[16 * (f - F0) + 2 * m + 1] += __uint_as_float(w[m] & 0xFFFF0000u);
+        }
+    };
+    constexpr uint32_t ONE_ZERO = 0x00003F80u;  // bf16 pair (1.0, 0.0)
+    const uint4 lo = ld_shared_v4(rb + sw);
+    if constexpr (K == 16) {
+        const uint4 hi = ld_shared_v4(rb + (16u ^ sw));
+        uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], kBf16One2);
+#pragma unroll
+        for (int f = F0; f < F1; ++f) {
+            uint32_t w[8];
+            if (f == 0) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m) w[m] = X[m];
+            } else if (f == 1) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m) w[m] = bmul2(bmul2(X[m], kBf16One2), X[m]);
+            } else if (f <= 8) {
+                const int d = f - 1;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t R = (d % 2 == 0)
+                                           ? X[(m + d / 2) & 7]
+                                           : __byte_perm(X[(m + (d - 1) / 2) & 7], X[(m + (d + 1) / 2) & 7], 0x5432);
+                    w[m] = bmul2(X[m], R);
+                }
+            } else {
+                w[0] = bmul2(X[0], X[4]);
+                w[1] = bmul2(X[1], X[5]);
+                w[2] = bmul2(X[2], X[6]);
+                w[3] = bmul2(X[3], X[7]);
+                w[4] = ONE_ZERO;
+                w[5] = w[6] = w[7] = 0u;
+            }
+            put(f, w);
+        }
+    } else {
+        uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], kBf16One2);
+#pragma unroll
+        for (int f = F0; f < F1; ++f) {
+            uint32_t w[8];
+            if (f == 0) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    w[m] = X[m];
+                    w[4 + m] = bmul2(bmul2(X[m], kBf16One2), X[m]);
+                }
+            } else if (f == 1) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    w[m] = bmul2(X[m], __byte_perm(X[m], X[(m + 1) & 3], 0x5432));
+                    w[4 + m] = bmul2(X[m], X[(m + 1) & 3]);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    w[m] = bmul2(X[m], __byte_perm(X[(m + 1) & 3], X[(m + 2) & 3], 0x5432));
+                w[4] = bmul2(X[0], X[2]);
+                w[5] = bmul2(X[1], X[3]);
+                w[6] = ONE_ZERO;
+                w[7] = 0u;
+            }
+            put(f, w);
+        }
+    }
+}
+
+// Sums n values over the 32 lanes of a warp (v[0..n) per lane, fp32) by recursive halving: at
+// each step a lane keeps one half of its values, adds its partner's copy of that half and sends
+// the other half, so the warp moves about n values in total instead of 5 n. Where the count
+// turns odd the remaining lane bits are summed whole (those lanes then hold equal sums).
+// After the call lane l holds z_final_count(n, 16) sums of consecutive values from index base.
+__host__ __device__ constexpr int z_final_count(int n, int o) {
+    return o == 0 ? n : (n % 2 == 0 ? z_final_count(n / 2, o / 2) : z_final_count(n, o / 2));
+}
+// lane bits whose lanes hold duplicate sums (only the lane with those bits clear stores them)
+__host__ __device__ constexpr int z_dup_mask(int n, int o) {
+    return o == 0 ? 0 : (n % 2 == 0 ? z_dup_mask(n / 2, o / 2) : (o | z_dup_mask(n, o / 2)));
+}
+template <int NV, int n, int o>
+__device__ __forceinline__ void z_reduce_scatter(float (&v)[NV], int lane, int &base) {
+    if constexpr (o > 0) {
+        if constexpr (n % 2 == 0) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = up ? v[i] : v[i + n / 2];
+                const float keep = up ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+            }
+            if (up) base += n / 2;
+            z_reduce_scatter<NV, n / 2, o / 2>(v, lane, base);
+        } else {
+#pragma unroll
+            for (int i = 0; i < n; ++i) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
+            z_reduce_scatter<NV, n, o / 2>(v, lane, base);
+        }
+    }
+}
 
 // ------------------------------------------------------------------------------------------------
 // Work partition. The heads are dealt into L lanes (lane r: heads h = r, r + L, ...), and each
@@ -1260,9 +1383,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_st_x1(tmem + lo + CF::TM_Z + 16, __float_as_uint(zb));
                 }
             };
-            static_assert(kMaxChain == 2, "one prefix load path per chain length");
+            static_assert(kMaxChain == 4, "one prefix load path per chain length");
             if (m == 1) load_prefix(std::integral_constant<int, 1>{});
-            else load_prefix(std::integral_constant<int, 2>{});
+            else if (m == 2) load_prefix(std::integral_constant<int, 2>{});
+            else if (m == 3) load_prefix(std::integral_constant<int, 3>{});
+            else load_prefix(std::integral_constant<int, 4>{});
             tmem_wait_st();
             convert(cidx++, 63);
         }
@@ -1297,17 +1422,19 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // chunks of pieces cta_first[j] .. cta_first[j + 1] - 1 in order, into two TMEM accumulators used
 // in turn, so that one piece's slot is written while the next piece is summed.
 // warp 0: TMA producer | warp 1: MMA issuer | warp 2: owns TMEM | warp 3: idle | warps 4-11: f(k)
-// tiles (half of each token row per warp) | warps 12-15: slot writers (512 threads; with 384, one
-// piece per CTA, warps 8-11 write the slot after building)
+// tiles (half of each token row per warp; V = 128: also z of each piece, summed in registers) |
+// warps 12-15: slot writers (512 threads; with 384, one piece per CTA, warps 8-11 write the slot
+// after building)
 // ------------------------------------------------------------------------------------------------
 // Barriers of the aggregate kernel with S k/v stages and NP f(k) buffers: TMA_FULL[S],
 // STAGE_FREE[S], PHIK_FULL[NP], PHIK_FREE[NP], per accumulator AGG_DONE[2] (its piece is summed)
-// and SLOT_READ[2] (its slot is written), DRAIN.
+// and SLOT_READ[2] (its slot is written), DRAIN, ZRED (V = 128: the builder warps' partial sums of
+// a piece's z are in shared memory).
 template <int S, int NP>
 struct AggBar {
     static constexpr int TMA_FULL0 = 0, STAGE_FREE0 = S, PHIK_FULL0 = 2 * S, PHIK_FREE0 = 2 * S + NP,
                          AGG_DONE0 = 2 * S + 2 * NP, SLOT_READ0 = AGG_DONE0 + 2, DRAIN = SLOT_READ0 + 2,
-                         COUNT = DRAIN + 1;
+                         ZRED = DRAIN + 1, COUNT = ZRED + 1;
     static_assert(8 * COUNT + 8 <= 256, "barrier area");
 };
 constexpr uint32_t kAggAccStride = 256;  // TMEM columns between the two accumulators
@@ -1400,7 +1527,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         for (int i = 0; i < AB_COUNT; ++i) {
             const bool phik_full = i >= AB_PHIK_FULL0 && i < AB_PHIK_FULL0 + NP;
             const bool slot_read = i >= AB_SLOT_READ0 && i < AB_SLOT_READ0 + 2;
-            mbar_init(BAR(i), phik_full ? 8u : (slot_read ? 4u : 1u));
+            mbar_init(BAR(i), (phik_full || i == AB::ZRED) ? 8u : (slot_read ? 4u : 1u));
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -1418,10 +1545,6 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         if (threadIdx.x < 16)
             st_shared_u16(sb + CF::A_OFF_ONES + sw128(threadIdx.x, 0), 0x3F80);
     }
-    if (threadIdx.x < 32)
-        st_shared_v4(sb + CF::A_OFF_ZONES + 16u * threadIdx.x, threadIdx.x < 2 ? 0x3F803F80u : 0u,
-                     threadIdx.x < 2 ? 0x3F803F80u : 0u, threadIdx.x < 2 ? 0x3F803F80u : 0u,
-                     threadIdx.x < 2 ? 0x3F803F80u : 0u);
     // one accumulator (256 columns) when the CTA sums one piece, else two
     const uint32_t tmem_cols = p1 - p0 > 1 ? 2 * kAggAccStride : kAggAccStride;
     if (warp == 2) {
@@ -1457,8 +1580,6 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t ID_UPD = idesc_bf16_f32(128, CF::PP, 1, 1);
-            constexpr uint32_t ID_Z = idesc_bf16_f32(128, 16, 1, 0);
-            const uint64_t d_zones = smem_desc(sb + CF::A_OFF_ZONES, 16, 256, LAYOUT_SW32);
             PieceWalk w;
             w.init(ap, p0, p1, n_c, Hl, L, r_lane);
             int kk = 0;  // pieces of this CTA started
@@ -1472,20 +1593,16 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                 if (!wait_bar(BAR(AB_PHIK_FULL0 + pb), (u / NP) & 1, abort_flag, SITE_PHIK_FULL)) break;
                 BASED_TRACE_EV(u + 40, 1);
                 tc_fence_after();
-                const uint32_t t_s = tmem + b * kAggAccStride, t_z = t_s + CF::TA_Z;
+                const uint32_t t_s = tmem + b * kAggAccStride;
                 const uint32_t lbo_a = CF::ZROW ? (CF::A_OFF_ONES - (CF::A_OFF_V + s * CF::VT)) : 16384u;
                 const uint64_t d_va = smem_desc(sb + CF::A_OFF_V + s * CF::VT, lbo_a, 1024, LAYOUT_SW128);
                 const uint64_t d_phik = smem_desc(sb + CF::A_OFF_PHIK + pb * CF::PHI, 4096, 256, LAYOUT_SW32);
                 const bool carry = !w.first();
+                // (V = 128: z is summed by the builders, not by an MMA)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t acc = (j > 0 || carry) ? 1u : 0u;
                     mma_ss(t_s, v_step<CF::ZROW>(d_va, j), dadd(d_phik, 512 * j), ID_UPD, acc);
-                    if constexpr (!CF::ZROW) {
-                        mma_ss(t_z, dadd(d_phik, 512 * j), d_zones, ID_Z, acc);
-                        if constexpr (CF::PP > 128)
-                            mma_ss(t_z + 16, dadd(d_phik, 2 * 4096 + 512 * j), d_zones, ID_Z, acc);
-                    }
                 }
                 mma_commit(BAR(AB_PHIK_FREE0 + pb));
                 mma_commit(BAR(AB_STAGE_FREE0 + s));
@@ -1505,23 +1622,84 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // feature builders (warps 4-11): token t of the chunk, warps 4-7 the first half of its
         // feature blocks and warps 8-11 the second half, cycling through the f(k) buffers
         const int t = (warp & 3) * 32 + lane;
-        const int f_lo = warp < 8 ? 0 : (CF::NBLK + 1) / 2, f_hi = warp < 8 ? (CF::NBLK + 1) / 2 : CF::NBLK;
-        for (int u = 0; u < nchunks; ++u) {
-            const int s = u % S, pb = u % NP;
-            if (!wait_bar(BAR(AB_TMA_FULL0 + s), (u / S) & 1, abort_flag, SITE_TMA_FULL)) break;
-            if (u >= NP && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((u / NP) - 1) & 1, abort_flag,
-                                     SITE_PHIK_FREE))
-                break;
-            if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 3);
-            build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
-                              kBf16One2, kBf16One2, f_lo, f_hi);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
-            if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 4);
+        constexpr int H0 = (CF::NBLK + 1) / 2;  // feature blocks of the first half of a row
+        if constexpr (CF::ZROW) {
+            const int f_lo = warp < 8 ? 0 : H0, f_hi = warp < 8 ? H0 : CF::NBLK;
+            for (int u = 0; u < nchunks; ++u) {
+                const int s = u % S, pb = u % NP;
+                if (!wait_bar(BAR(AB_TMA_FULL0 + s), (u / S) & 1, abort_flag, SITE_TMA_FULL)) break;
+                if (u >= NP && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((u / NP) - 1) & 1, abort_flag,
+                                         SITE_PHIK_FREE))
+                    break;
+                if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 3);
+                build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
+                                  kBf16One2, kBf16One2, f_lo, f_hi);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
+                if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 4);
+            }
+        } else {
+            // V = 128: the builders also sum z = sum f(k) of each piece: per thread over its
+            // tokens, then over the warp's lanes, then over the four warps of its half of the row
+            // (through shared memory), into the slot's z column
+            auto build_sum = [&](auto half) {
+                constexpr int F0 = decltype(half)::value ? H0 : 0;
+                constexpr int F1 = decltype(half)::value ? CF::NBLK : H0;
+                constexpr int NZ = (F1 - F0) * 16;
+                float *red = reinterpret_cast<float *>(smem + CF::A_OFF_ZRED);
+                float z[NZ];
+#pragma unroll
+                for (int i = 0; i < NZ; ++i) z[i] = 0.0f;
+                PieceWalk w;
+                w.init(ap, p0, p1, n_c, Hl, L, r_lane);
+                int kk = 0;
+                for (int u = 0; u < nchunks; ++u, w.next()) {
+                    const int s = u % S, pb = u % NP;
+                    if (!wait_bar(BAR(AB_TMA_FULL0 + s), (u / S) & 1, abort_flag, SITE_TMA_FULL)) break;
+                    if (u >= NP && !wait_bar(BAR(AB_PHIK_FREE0 + pb), ((u / NP) - 1) & 1, abort_flag,
+                                             SITE_PHIK_FREE))
+                        break;
+                    if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 3);
+                    build_k_features_acc<K, F0, F1>(sb + CF::A_OFF_RAWK + s * CF::RAW,
+                                                    sb + CF::A_OFF_PHIK + pb * CF::PHI, t, z);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));
+                    if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 4);
+                    if (!w.last()) continue;
+                    // piece kk is built: its z
+                    int zbase = 0;
+                    z_reduce_scatter<NZ, NZ, 16>(z, lane, zbase);
+                    // partials of warp (half, q4) in buffer kk % 2: [buffer][half][q4][H0 * 16]
+                    float *mine = red + ((kk & 1) * 8 + decltype(half)::value * 4 + (warp & 3)) * (H0 * 16);
+                    constexpr int NF = z_final_count(NZ, 16);
+                    if ((lane & z_dup_mask(NZ, 16)) == 0) {
+#pragma unroll
+                        for (int i = 0; i < NF; ++i) mine[zbase + i] = z[i];
+                    }
+#pragma unroll
+                    for (int i = 0; i < NZ; ++i) z[i] = 0.0f;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(AB::ZRED));
+                    if (!wait_bar(BAR(AB::ZRED), kk & 1, abort_flag, SITE_ZRED)) break;
+                    // feature c of the row: the four warps' partials of its half
+                    const int tb = (warp - 4) * 32 + lane;  // 0..255
+                    if (tb < CF::PP) {
+                        const int hf = tb < H0 * 16 ? 0 : 1, ci = tb - hf * H0 * 16;
+                        const float *part = red + ((kk & 1) * 8 + hf * 4) * (H0 * 16) + ci;
+                        const float zc = (part[0] + part[H0 * 16]) + (part[2 * H0 * 16] + part[3 * H0 * 16]);
+                        slots[static_cast<size_t>(p0 + kk) * CF::SLOT + static_cast<size_t>(tb) * CF::SROWS + V] = zc;
+                    }
+                    ++kk;
+                }
+            };
+            if (warp < 8) build_sum(std::integral_constant<int, 0>{});
+            else build_sum(std::integral_constant<int, 1>{});
         }
     }
-    // Slot writers: S^T rows (and z) of each summed piece -> its fp32 slot, element (c, r) at
+    // Slot writers: S^T rows (V = 64: and z, row 64) of each summed piece -> its fp32 slot (V = 128:
+    // the builders write z), element (c, r) at
     // c * SROWS + r. With several pieces per CTA they are warps 12-15 (512 threads), so that the
     // f(k) builders never wait for a slot; with one piece per CTA (384 threads) warps 8-11 write it
     // after building.
@@ -1557,16 +1735,6 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                         }
                     }
                 }
-            }
-            if constexpr (!CF::ZROW) {
-                uint32_t za, zb;
-                tmem_ld_x1(acc + CF::TA_Z, za);
-                tmem_ld_x1(acc + CF::TA_Z + 16, zb);
-                tmem_wait_ld();
-                float *zcol = slot + V;  // element (c, V) at c * SROWS + V
-                if (r < CF::PP && r < 128) zcol[static_cast<size_t>(r) * CF::SROWS] = __uint_as_float(za);
-                if (r + 32 >= 128 && r + 32 < CF::PP)
-                    zcol[static_cast<size_t>(r + 32) * CF::SROWS] = __uint_as_float(zb);
             }
             tc_fence_before();
             __syncwarp();

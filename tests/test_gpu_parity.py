@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from linear_attention_gb300.based import (BasedError, based_fwd, based_fwd_host, device_status,
-                                          selftest_wait_timeout, workspace_size)
+                                          kernel_count, selftest_wait_timeout, workspace_size)
 from linear_attention_gb300.inputs import GRADER_WORKLOADS, WORKLOADS, make_inputs, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -70,7 +70,7 @@ SMALL = [
     (2, 700, 3, 8, 128, 21, 0.3),
     (1, 1536, 1, 16, 128, 22, None),
     (2, 4096, 8, 8, 64, 23, None),
-    # the forward kernel sums up to two partial states into a prefix itself (no scan kernel)
+    # the forward kernel sums the partial states of a prefix itself (no scan kernel)
     (1, 1100, 64, 16, 64, 24, None),
     (3, 1500, 40, 8, 128, 25, 0.3),
     (3, 1024, 24, 8, 64, 26, None),
@@ -84,6 +84,30 @@ def test_small_shapes_match_oracle(B, T, H, K, V, seed, scale, cuda_device):
     q, k, v = make_inputs(B, T, H, K, V, seed)
     o = _run_gpu(q, k, v, scale, cuda_device)
     ref, _ = oracle.chunked(q, k, v, _scale(K, scale), chunk=64)
+    _assert_close(o, ref, (B, T, H, K, V))
+
+
+# Both prefix paths, with the kernel count they launch on a 152-SM GB300: the forward kernel sums
+# up to four partial states into a prefix itself (aggregate + forward); longer chains of partial
+# states are summed by the scan kernel first (aggregate + scan + forward).
+PREFIX_PATHS = [
+    # B, T, H, K, V, seed, kernels
+    (1, 1024, 32, 16, 128, 50, 2),  # prefixes of up to four slots
+    (2, 1024, 16, 16, 64, 51, 2),   # prefixes of up to four slots
+    (1, 512, 32, 8, 128, 52, 2),    # up to three slots, eight head lanes
+    (1, 2048, 4, 16, 128, 53, 3),   # one head per lane cut into many ranges: scan
+    (1, 2048, 8, 8, 64, 54, 3),
+]
+
+
+@pytest.mark.parametrize("B,T,H,K,V,seed,kernels", PREFIX_PATHS,
+                         ids=[f"B{c[0]}T{c[1]}H{c[2]}K{c[3]}V{c[4]}" for c in PREFIX_PATHS])
+def test_prefix_paths_match_oracle(B, T, H, K, V, seed, kernels, cuda_device):
+    if torch.cuda.get_device_properties(cuda_device).multi_processor_count == 152:
+        assert kernel_count(B, T, H, K, V) == kernels
+    q, k, v = make_inputs(B, T, H, K, V, seed)
+    o = _run_gpu(q, k, v, None, cuda_device)
+    ref, _ = oracle.chunked(q, k, v, _scale(K, None), chunk=64)
     _assert_close(o, ref, (B, T, H, K, V))
 
 
