@@ -384,7 +384,7 @@ def run_gpu(args, w, world, rank, local):
             "l2": f"{nsets} rotating input/output sets ({nsets * wbytes / 2**20:.0f} MiB > 3x L2)",
             "output": "bf16" if obf else "fp32",
             "launch": f"stream launches, one {'based_fwd_bf16_out' if obf else 'based_fwd'} call per step "
-                      f"({launches} kernel(s): aggregate, scan when a prefix chains more than two "
+                      f"({launches} kernel(s): aggregate, scan when a prefix chains more than four "
                       "partial states, forward; the later ones as programmatic dependents)"}),
         "tflops": flops / (ms_per_step * 1e-3) / 1e12,
         "pct_bf16_peak": 100.0 * flops / (ms_per_step * 1e-3) / (tc * 1e12),
