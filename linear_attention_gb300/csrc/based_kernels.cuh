@@ -1511,16 +1511,20 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::A_OFF_BAR + 8 * AB_COUNT + 4);
     auto BAR = [&](int i) -> uint32_t { return sb + CF::A_OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
-    // k, v tiles of the CTA's chunk u (cursor position cu) into stage u % S, completing on TMA_FULL
+    // k, v tiles of the CTA's chunk u (cursor position cu) into stage u % S, completing on TMA_FULL.
+    // Their L2 lines are marked for eviction first: this pass reads them once, and without the mark
+    // they push out the slots written earlier in the pass, which the forward kernel reads next
+    // (measured: 0.4 - 1.1 % faster calls on B=4..8 T=16384 H=32).
     auto issue_loads = [&](int u, const Cursor &cu) {
         const int s = u % S;
         const uint32_t bar = BAR(AB_TMA_FULL0 + s);
+        const uint64_t pol = l2_policy_evict_first();
         BASED_TRACE_EV(u + 40, 0);
         mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
-        tma_load_4d(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
-        tma_load_4d(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
+        tma_load_4d_hint(sb + CF::A_OFF_RAWK + s * CF::RAW, &tm_k, bar, 0, cu.h, cu.t0(), cu.b, pol);
+        tma_load_4d_hint(sb + CF::A_OFF_V + s * CF::VT, &tm_v, bar, 0, cu.h, cu.t0(), cu.b, pol);
         if constexpr (V == 128)
-            tma_load_4d(sb + CF::A_OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(), cu.b);
+            tma_load_4d_hint(sb + CF::A_OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(), cu.b, pol);
     };
     const int n_early = nchunks < S ? nchunks : S;  // loads issued during set-up
     if (threadIdx.x == 0) {
