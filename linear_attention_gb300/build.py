@@ -11,6 +11,7 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libbased_gb300.so")
 SOURCES = [os.path.join(CSRC, "based_fwd.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "based_kernels.cuh"), os.path.join(CSRC, "sm103_ptx.cuh"),
+                  os.path.join(CSRC, "based_plan.h"),
                   os.path.join(ROOT, "include", "based.h")]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared", "-Xcompiler", "-fvisibility=hidden"]

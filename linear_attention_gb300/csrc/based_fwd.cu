@@ -13,6 +13,7 @@
 
 #include "../../include/based.h"
 #include "based_kernels.cuh"
+#include "based_plan.h"
 
 namespace {
 
@@ -136,12 +137,11 @@ int slot_floats(int K, int V) { return (V + 1) * ((K == 16) ? 160 : 48); }
 // piece, up to about twice the ranges; with less it falls back to one slot per range)
 Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~static_cast<size_t>(0)) {
     Plan p;
-    p.n_c = (T + kChunk - 1) / kChunk;
-    const long long n_all = static_cast<long long>(B) * H * p.n_c;
-    p.L = choose_lanes(K, H, n_all, sms);
-    p.N = n_all / p.L;
-    const int gmax = sms / p.L < kMaxRanges ? sms / p.L : kMaxRanges;
-    p.G = static_cast<int>(p.N < gmax ? p.N : gmax);
+    const LaneSplit ls = lane_split(B, T, H, K, sms);
+    p.n_c = ls.n_c;
+    p.L = ls.L;
+    p.N = ls.N;
+    p.G = ls.G;
     p.need_agg = false;
     for (int i = 0; i < p.G; ++i)
         if (has_aggregate(p.N, p.G, i, p.n_c)) p.need_agg = true;

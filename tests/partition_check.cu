@@ -13,7 +13,7 @@
 #include <cstdio>
 #include <vector>
 
-#include "../linear_attention_gb300/csrc/based_kernels.cuh"
+#include "../linear_attention_gb300/csrc/based_plan.h"
 
 using namespace based;
 
@@ -48,13 +48,14 @@ int main() {
             for (int B : {1, 3}) {
                 for (int H : {1, 2, 3, 5, 12, 16, 40, 64}) {
                     for (int T : {1, 64, 127, 128, 129, 300, 1000, 3000, 4096, 16384}) {
-                        const int n_c = (T + kChunk - 1) / kChunk;
+                        // the split the library's plan uses
+                        const LaneSplit ls = lane_split(B, T, H, K, sms);
+                        const int n_c = ls.n_c, L = ls.L, G = ls.G;
+                        const long long N = ls.N;
                         const long long n_all = 1ll * B * H * n_c;
-                        const int L = choose_lanes(K, H, n_all, sms);
+                        if (n_c != (T + kChunk - 1) / kChunk || N * L != n_all) { printf("bad split\n"); return 1; }
                         if (L < 1 || H % L != 0 || L > 128 / (2 * K)) { printf("bad lanes\n"); return 1; }
-                        const long long N = n_all / L;
-                        const int gmax = sms / L < kMaxRanges ? sms / L : kMaxRanges;
-                        const int G = static_cast<int>(N < gmax ? N : gmax);
+                        if (G < 1 || G > kMaxRanges || G > N || G * L > sms) { printf("bad range count\n"); return 1; }
                         const int g1 = static_cast<int>(n_all < sms ? n_all : (sms < kMaxRanges ? sms : kMaxRanges));
                         if (G * L < g1) {
                             printf("lanes leave SMs idle: sms=%d K=%d B=%d H=%d T=%d\n", sms, K, B, H, T);
