@@ -23,13 +23,18 @@
  *     first call on a device (or a call that needs a larger workspace than any before it)
  *     allocates the library-owned workspace with cudaMalloc.
  *   - Return value: 0 on success or a negative BASED_ERR_* code. Argument errors are detected
- *     on the host before anything is launched. based_strerror() names every code.
+ *     on the host before anything is launched. based_fwd_strerror() names every code.
  *
  * Ownership: the caller owns q, k, v, o. The library owns one workspace per device, which holds
  * per-segment partial states (fp32) for the chunk-parallel state scan; it lives until process
- * exit. Concurrent calls that use the library-owned workspace on the same device must be
- * ordered by the caller (same stream, or events); based_fwd_ws() takes a caller-owned workspace
- * instead and has no such restriction.
+ * exit. The library allocates no device memory per call, with one exception: based_fwd (and
+ * based_fwd_timed, and based_fwd_bf16_out with a NULL workspace) grow the library-owned
+ * workspace with cudaMalloc when a shape needs more than any call before it. A workspace that a
+ * larger one replaces is never freed, so that a CUDA graph which captured an earlier call still
+ * replays into valid memory. Callers that must not allocate at all use based_fwd_ws (caller-owned
+ * workspace) or based_fwd_noalloc (fixed scratch). Concurrent calls that use the library-owned
+ * workspace on the same device must be ordered by the caller (same stream, or events);
+ * based_fwd_ws() takes a caller-owned workspace instead and has no such restriction.
  */
 #ifndef BASED_GB300_H
 #define BASED_GB300_H
@@ -142,6 +147,9 @@ BASED_API int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint
  * before returning. Page-locked host memory makes the copies asynchronous DMA; pageable memory
  * also works, more slowly. The device buffers, streams, events and workspace are cached per
  * device and grown on demand (cudaMalloc), so this call is not reentrant for one device.
+ * After its final synchronisation the call reads and clears the device status word
+ * (based_device_status): if any kernel of this library gave up a bounded wait since the word was
+ * last cleared, it returns BASED_ERR_DEVICE_TIMEOUT, and o_host must not be used.
  */
 BASED_API int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_t *v_host, int B,
                    int T, int H, int K, int V, float scale, float *o_host, based_stream_t stream);
@@ -166,12 +174,17 @@ BASED_API int based_fwd_kernel_count(int B, int T, int H, int K, int V);
 BASED_API int based_device_status(int device, unsigned int *status, int clear);
 
 /* Launches a one-thread kernel that waits on a barrier nothing ever signals, with the given
- * limit in nanoseconds (clamped to [1e3, 2e9]), and returns after it gave up; the status word
- * then reports a timeout at site 255. Exercises the bounded-wait path without hanging the GPU.
- * Synchronous. Returns 0 if the wait timed out as expected, else an error code. */
+ * limit in nanoseconds (clamped to [1e3, 2e9]), and returns after it gave up. The status word is
+ * cleared before the launch and left reporting a timeout at site 255 afterwards, so that a caller
+ * can check how other entry points report it; clear it with based_device_status(dev, &s, 1).
+ * Exercises the bounded-wait path without hanging the GPU. Synchronous. Returns 0 if the wait
+ * timed out as expected, else an error code. */
 BASED_API int based_selftest_wait_timeout(unsigned long long limit_ns);
 
-/* Human-readable name of a return code. */
+/* Human-readable name of a return code (a static string; never NULL). */
+BASED_API const char *based_fwd_strerror(int code);
+
+/* The same as based_fwd_strerror (the name earlier versions of this library exported). */
 BASED_API const char *based_strerror(int code);
 
 /* The last CUDA error string seen by the library on this thread ("" if none). */

@@ -59,6 +59,8 @@ def _load():
     L.based_device_status.restype = i
     L.based_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong]
     L.based_selftest_wait_timeout.restype = i
+    L.based_fwd_strerror.argtypes = [i]
+    L.based_fwd_strerror.restype = ctypes.c_char_p
     L.based_strerror.argtypes = [i]
     L.based_strerror.restype = ctypes.c_char_p
     L.based_last_cuda_error.argtypes = []
@@ -77,7 +79,7 @@ def library():
 def _check(rc: int, what: str):
     if rc != 0:
         L = _load()
-        msg = L.based_strerror(rc).decode()
+        msg = L.based_fwd_strerror(rc).decode()
         cuda = L.based_last_cuda_error().decode()
         raise BasedError(f"{what} failed: {msg} ({rc})" + (f": {cuda}" if cuda else ""))
 
@@ -232,5 +234,7 @@ def device_status(device: int = 0, clear: bool = False) -> int:
 
 
 def selftest_wait_timeout(limit_ns: int = 20_000_000) -> None:
+    """Runs the bounded-wait self-test; the device status word is left reporting its timeout
+    (site 255) until it is cleared with device_status(dev, clear=True)."""
     L = _load()
     _check(L.based_selftest_wait_timeout(limit_ns), "based_selftest_wait_timeout")

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/based.h"
 #include "based_kernels.cuh"
@@ -101,6 +102,9 @@ struct DeviceState {
     bool attrs_done[2][2][2] = {};  // [K == 16][V == 128][bf16 output]
     void *ws = nullptr;
     size_t ws_bytes = 0;
+    // Workspaces that a larger one replaced. They are never freed: a CUDA graph may have captured
+    // a call that uses one, and replaying it must not write to freed memory.
+    std::vector<void *> retired_ws;
     void *hbuf = nullptr;  // based_fwd_host staging (q | k | v | o)
     size_t hbuf_bytes = 0;
     // based_fwd_host pipeline: copy-in, compute and copy-out streams, per-piece events, and the
@@ -268,13 +272,10 @@ int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, i
     if (own_ws) {
         std::lock_guard<std::mutex> lk(d.m);
         if (p.ws_bytes > d.ws_bytes) {
-            if (d.ws) {
-                cudaError_t e = cudaFree(d.ws);
-                d.ws = nullptr;
-                d.ws_bytes = 0;
-                if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-            }
-            BASED_CUDA(cudaMalloc(&d.ws, p.ws_bytes));
+            void *w = nullptr;
+            BASED_CUDA(cudaMalloc(&w, p.ws_bytes));
+            if (d.ws) d.retired_ws.push_back(d.ws);  // kept: a captured graph may still use it
+            d.ws = w;
             d.ws_bytes = p.ws_bytes;
         }
         ws = d.ws;
@@ -501,7 +502,11 @@ int based_fwd_host(const uint16_t *q_host, const uint16_t *k_host, const uint16_
     BASED_CUDA(cudaEventRecord(d.hdone, d.hs_out));
     BASED_CUDA(cudaStreamWaitEvent(caller, d.hdone, 0));
     BASED_CUDA(cudaStreamSynchronize(caller));
-    return BASED_OK;
+    // The call has synchronised: report (and clear) a bounded wait that gave up since the status
+    // word was last cleared, so that a timed-out kernel never passes for a result.
+    unsigned int st = 0;
+    if ((rc = based_device_status(dev, &st, 1)) != BASED_OK) return rc;
+    return st != 0 ? BASED_ERR_DEVICE_TIMEOUT : BASED_OK;
 }
 
 int based_device_status(int device, unsigned int *status, int clear) {
@@ -537,14 +542,14 @@ int based_selftest_wait_timeout(unsigned long long limit_ns) {
     cudaFree(res);
     if (e != cudaSuccess) return cuda_fail(e, "selftest kernel");
     unsigned int st;
-    rc = based_device_status(dev, &st, 1);
+    rc = based_device_status(dev, &st, 0);  // left set: other entry points must report it
     if (rc != BASED_OK) return rc;
     // the wait must have given up (result 0) and recorded site 255
     if (h != 0 || (st & 1u) == 0u || ((st >> 8) & 0xFFu) != 255u) return BASED_ERR_BAD_ARGUMENT;
     return BASED_OK;
 }
 
-const char *based_strerror(int code) {
+const char *based_fwd_strerror(int code) {
     switch (code) {
         case BASED_OK: return "ok";
         case BASED_ERR_NULL_POINTER: return "null pointer";
@@ -563,6 +568,8 @@ const char *based_strerror(int code) {
         default: return "unknown error code";
     }
 }
+
+const char *based_strerror(int code) { return based_fwd_strerror(code); }
 
 const char *based_last_cuda_error(void) { return tl_cuda_error; }
 

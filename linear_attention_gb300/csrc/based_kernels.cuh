@@ -6,12 +6,13 @@
 // (q.k)^2/2 exactly), every head is cut into chunks of 128 rows and, per chunk c,
 //     s   = q_c k_c^T                              (tensor core -> TMEM, fp32)
 //     A   = 1 + sigma s + sigma^2 s^2 / 2, j <= i   (fp32 polynomial -> bf16 in TMEM)
-//     O   = A [v_c | 1] + f~(q_c) [S | z]          (tensor core; the ones column gives rowsum A,
+//     O   = A [v_c | 1] + f~(q_c) D [S | z]        (tensor core; the ones column gives rowsum A,
 //                                                    z gives the inter-chunk denominator)
 //     o   = O_num / (O_den + 1e-6)
 //     S  += v_c^T f(k_c),  z += f(k_c)^T 1         (tensor core, fp32 accumulation in TMEM)
-// where f~(q) = f(sigma q) carries the feature coefficients (1, 1, 1/2 on squares, 1 on cross
-// products). The per-head chunk sequence is split across CTAs; the state each CTA starts from is
+// where f~(q) carries the feature coefficients (1, 1, 1/2 on squares, 1 on cross products) and
+// D multiplies feature c of the fp32 state by sigma^degree(c) (1, sigma, sigma^2) as the state is
+// rounded to its bf16 operand, so that f~(q) D f(k) = 1 + sigma q.k + sigma^2 (q.k)^2 / 2. The per-head chunk sequence is split across CTAs; the state each CTA starts from is
 // the sum of the partial states of the chunks before it (aggregate pass + scan), so the forward
 // kernel never waits on another CTA.
 #pragma once
@@ -232,6 +233,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
 }
+// Two fp32 values (as a packed pair) times two fp32 factors in one packed multiply.
+__device__ __forceinline__ void mul_f32x2(float &a, float &b, uint64_t f) {
+    uint64_t x = pack_f32x2(a, b), y;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(f));
+    a = __uint_as_float(static_cast<uint32_t>(y));
+    b = __uint_as_float(static_cast<uint32_t>(y >> 32));
+}
 // bf16x2 of the Taylor weights 1 + c1 s + c2 s^2 for two fp32 scores, evaluated as
 // fma(s, fma(c2, s, c1), 1) on packed fp32 pairs (square kept in fp32).
 __device__ __forceinline__ uint32_t taylor2(uint32_t s_lo, uint32_t s_hi, uint64_t C2, uint64_t C1,
@@ -254,18 +262,20 @@ __device__ __forceinline__ uint32_t taylor2(uint32_t s_lo, uint32_t s_hi, uint64
 //         1, 0 x 7].
 // K = 8:  block 0 = [x, x_a^2], 1 = [x_a x_{a+1}, x_a x_{a+2}] (mod 8), 2 = [x_a x_{a+3} (mod 8),
 //         x_a x_{a+4} (a<4), 1, 0 x 3].
-// Every unordered pair a < b appears exactly once. x is first multiplied by sig2 and the squares
-// by half2 (bf16 pairs): (1, 1) and (1, 1) give f(k); (sigma, sigma) and (1/2, 1/2) give the
-// query side f~(q) = f(sigma q) with halved squares, so that f~(q).f(k) = 1 + sigma q.k +
-// sigma^2 (q.k)^2 / 2. (Multiplying by 1.0 is exact, so both sides share this one code path.)
-// Only blocks f_lo <= f < f_hi are built (two threads can share a token row).
+// Every unordered pair a < b appears exactly once. The squares are multiplied by half2 (a bf16
+// pair): (1, 1) gives f(k), (1/2, 1/2) the query side f~(q) with halved squares, so that
+// f~(q).f(k) = 1 + q.k + (q.k)^2 / 2 (a power of two is exact, so both sides share this one code
+// path). The scale is not applied to q: the state conversion multiplies feature c of the fp32
+// state by scale^degree(c) before the state is rounded to bf16, so that the scale enters once,
+// in fp32, and q is never rounded after scaling. Only blocks f_lo <= f < f_hi are built (two
+// threads can share a token row).
 // Out of line: the q and k builders share one copy of the code, which keeps the kernel's
 // instruction-cache footprint small.
 constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
 constexpr uint32_t kBf16Half2 = 0x3F003F00u;  // bf16 pair (0.5, 0.5)
 template <int K>
-__device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t sig2,
-                                            uint32_t half2, int f_lo, int f_hi) {
+__device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, uint32_t half2, int f_lo,
+                                            int f_hi) {
     const uint32_t rb = raw + static_cast<uint32_t>(t) * 32u;
     const uint32_t sw = static_cast<uint32_t>(((t >> 2) & 1) << 4);
     const uint4 lo = ld_shared_v4(rb + sw);
@@ -280,9 +290,7 @@ __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, u
     auto in = [&](int f) { return f_lo <= f && f < f_hi; };
     if constexpr (K == 16) {
         const uint4 hi = ld_shared_v4(rb + (16u ^ sw));
-        uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], sig2);
+        const uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
         if (in(0)) store_blk(0, X[0], X[1], X[2], X[3], X[4], X[5], X[6], X[7]);
         if (in(1))
             store_blk(1, sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]), sq(X[4]), sq(X[5]), sq(X[6]), sq(X[7]));
@@ -306,9 +314,7 @@ __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, u
             store_blk(9, bmul2(X[0], X[4]), bmul2(X[1], X[5]), bmul2(X[2], X[6]), bmul2(X[3], X[7]),
                       ONE_ZERO, 0u, 0u, 0u);
     } else {
-        uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], sig2);
+        const uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
         if (in(0)) store_blk(0, X[0], X[1], X[2], X[3], sq(X[0]), sq(X[1]), sq(X[2]), sq(X[3]));
         uint32_t R1[4], R3[4];
 #pragma unroll
@@ -326,9 +332,9 @@ __device__ __noinline__ void build_features(uint32_t raw, uint32_t phi, int t, u
 }
 
 // f(k) of token t for feature blocks [F0, F1) (half of the row, fixed at compile time), stored as
-// build_features stores it (the same products, bit for bit), with every feature also added to
-// z[16 (f - F0) + j] (fp32; feature j of block f), so that the aggregate pass gets z = sum f(k)
-// without an MMA.
+// build_features stores it with half2 = (1, 1) (the same products, bit for bit), with every
+// feature also added to z[16 (f - F0) + j] (fp32; feature j of block f), so that the aggregate
+// pass gets z = sum f(k) without an MMA.
 template <int K, int F0, int F1>
 __device__ __forceinline__ void build_k_features_acc(uint32_t raw, uint32_t phi, int t, float (&z)[(F1 - F0) * 16]) {
     const uint32_t rb = raw + static_cast<uint32_t>(t) * 32u;
@@ -347,9 +353,7 @@ __device__ __forceinline__ void build_k_features_acc(uint32_t raw, uint32_t phi,
     const uint4 lo = ld_shared_v4(rb + sw);
     if constexpr (K == 16) {
         const uint4 hi = ld_shared_v4(rb + (16u ^ sw));
-        uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int m = 0; m < 8; ++m) X[m] = bmul2(X[m], kBf16One2);
+        const uint32_t X[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
         for (int f = F0; f < F1; ++f) {
             uint32_t w[8];
@@ -358,7 +362,7 @@ __device__ __forceinline__ void build_k_features_acc(uint32_t raw, uint32_t phi,
                 for (int m = 0; m < 8; ++m) w[m] = X[m];
             } else if (f == 1) {
 #pragma unroll
-                for (int m = 0; m < 8; ++m) w[m] = bmul2(bmul2(X[m], kBf16One2), X[m]);
+                for (int m = 0; m < 8; ++m) w[m] = bmul2(X[m], X[m]);
             } else if (f <= 8) {
                 const int d = f - 1;
 #pragma unroll
@@ -379,9 +383,7 @@ __device__ __forceinline__ void build_k_features_acc(uint32_t raw, uint32_t phi,
             put(f, w);
         }
     } else {
-        uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) X[m] = bmul2(X[m], kBf16One2);
+        const uint32_t X[4] = {lo.x, lo.y, lo.z, lo.w};
 #pragma unroll
         for (int f = F0; f < F1; ++f) {
             uint32_t w[8];
@@ -389,7 +391,7 @@ __device__ __forceinline__ void build_k_features_acc(uint32_t raw, uint32_t phi,
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     w[m] = X[m];
-                    w[4 + m] = bmul2(bmul2(X[m], kBf16One2), X[m]);
+                    w[4 + m] = bmul2(X[m], X[m]);
                 }
             } else if (f == 1) {
 #pragma unroll
@@ -1085,7 +1087,6 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int t = (warp - 8) * 32 + lane;  // token of the chunk = TMEM lane = output row
         const int q4 = warp & 3;
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
-        const uint32_t sig2 = pack_bf16x2(scale, scale);
         int ro_idx = 0, upd_idx = 0;
         bool ok = true;
 
@@ -1179,8 +1180,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !wait_bar(BAR(FB_PHIQ_FREE), (ro_idx - 1) & 1, abort_flag, SITE_PHIQ_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_BEGIN);
-            build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, sig2, kBf16Half2, 0,
-                              CF::NBLK);
+            build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, kBf16Half2, 0, CF::NBLK);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIQ_FULL));
@@ -1193,8 +1193,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !wait_bar(BAR(FB_PHIK_FREE), (upd_idx - 1) & 1, abort_flag, SITE_PHIK_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIK_BEGIN);
-            build_features<K>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, kBf16One2, kBf16One2, 0,
-                              CF::NBLK);
+            build_features<K>(sb + CF::OFF_RAWK + s * CF::RAW, sb + CF::OFF_PHIK, t, kBf16One2, 0, CF::NBLK);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIK_FULL));
@@ -1241,27 +1240,43 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // One block of a state row as bf16: rows r < V are S^T rows; with the z row (V = 64) row V
         // is z rounded to bf16 and row V + 1 its rounding remainder (z as a hi/lo pair, about 16
         // significant bits). One code path for both kinds of row keeps the code small.
-        auto put_block = [&](uint32_t sbf, int f, const uint32_t *x) {
+        // The scale enters here, once, in fp32: feature c of the state is multiplied by
+        // scale^degree(c) as the state is rounded to its bf16 operand, i.e. by scale for the K
+        // linear features (c < K), by 1 for the constant feature (kConst: K = 16 block 9 column 8,
+        // K = 8 block 2 column 12) and by scale^2 for every square and cross product; with the
+        // query features f~(q) this gives 1 + scale q.k + scale^2 (q.k)^2 / 2.
+        const uint64_t S11 = pack_f32x2(scale, scale), S22 = pack_f32x2(scale * scale, scale * scale);
+        const uint64_t SC2 = pack_f32x2(1.0f, scale * scale);  // the pair that holds the constant feature
+        constexpr int kConst = K == 16 ? 9 * 16 + 8 : 2 * 16 + 12;
+        auto put_block = [&](uint32_t sbf, int f, const uint32_t *xs) {
             const uint32_t blk = sbf + CF::SBF_BLK * f;
             if (r <= LAST_ROW) {
+                float x[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(xs[j]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int p0 = 16 * f + 2 * j;
+                    mul_f32x2(x[2 * j], x[2 * j + 1], p0 < K ? S11 : (p0 == kConst ? SC2 : S22));
+                }
                 uint32_t hi[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    hi[j] = pack_bf16x2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                for (int j = 0; j < 8; ++j) hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
                 st_shared_v4(blk + sw32(r, 0), hi[0], hi[1], hi[2], hi[3]);
                 st_shared_v4(blk + sw32(r, 1), hi[4], hi[5], hi[6], hi[7]);
                 if (CF::ZROW && r == V) {
                     uint32_t lw[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        lw[j] = pack_bf16x2(__uint_as_float(x[2 * j]) - __uint_as_float(hi[j] << 16),
-                                            __uint_as_float(x[2 * j + 1]) - __uint_as_float(hi[j] & 0xFFFF0000u));
+                        lw[j] = pack_bf16x2(x[2 * j] - __uint_as_float(hi[j] << 16),
+                                            x[2 * j + 1] - __uint_as_float(hi[j] & 0xFFFF0000u));
                     st_shared_v4(blk + sw32(V + 1, 0), lw[0], lw[1], lw[2], lw[3]);
                     st_shared_v4(blk + sw32(V + 1, 1), lw[4], lw[5], lw[6], lw[7]);
                 }
             }
         };
         auto put_z = [&](uint32_t sbf, int p, float z) {
+            z *= p < K ? scale : (p == kConst ? 1.0f : scale * scale);
             const int f = p >> 4, j = p & 15;
             const __nv_bfloat16 h = __float2bfloat16_rn(z);
             const __nv_bfloat16 l = __float2bfloat16_rn(z - __bfloat162float(h));
@@ -1637,7 +1652,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     break;
                 if (warp == 4 && lane == 0) BASED_TRACE_EV(u + 40, 3);
                 build_features<K>(sb + CF::A_OFF_RAWK + s * CF::RAW, sb + CF::A_OFF_PHIK + pb * CF::PHI, t,
-                                  kBf16One2, kBf16One2, f_lo, f_hi);
+                                  kBf16One2, f_lo, f_hi);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(AB_PHIK_FULL0 + pb));

@@ -33,6 +33,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// Invalidates an mbarrier whose phases are all complete, so that its memory may be used for
+// something else (the fused kernel's second phase reuses the first phase's shared memory).
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 // Non-blocking test of a phase (no suspension): true if the phase with this parity has completed.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -301,6 +306,27 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return r;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Global-memory flags between CTAs of one grid (gpu scope)
+// ------------------------------------------------------------------------------------------------
+// Adds v with release semantics: every write this thread made before (and, through a preceding
+// fence and barrier, the writes of the threads it synchronised with) is visible to a thread that
+// observes the new value with an acquire load.
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Adds v with acquire-release semantics and returns the old value.
+__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 // Streaming 16-byte global store (the output is written once and not re-read).

@@ -29,7 +29,7 @@
  * Inputs are fp64 arrays (callers convert the exact bf16 values). Layouts follow the spec's
  * contract: q,k (B,T,H,K) and v (B,T,H,V), row-major and contiguous. Outputs are fp64.
  *
- * Readings where the spec is silent (all also listed in the design notes):
+ * Readings where the spec is silent (spec_md and contract_md fix none of these):
  *   - the scale is used as given (the caller passes the fp32 value the kernel receives);
  *   - T need not be a multiple of 64 or of the chunk length: the last chunk is short;
  *   - the output is returned in fp64 and compared against the kernel's fp32 output.

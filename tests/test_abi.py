@@ -30,7 +30,8 @@ def lib():
 def test_header_declares_entry_points():
     names = declared_functions()
     for n in ("based_fwd", "based_fwd_ws", "based_fwd_workspace_size", "based_fwd_host",
-              "based_strerror", "based_device_status", "based_selftest_wait_timeout"):
+              "based_fwd_strerror", "based_strerror", "based_device_status",
+              "based_selftest_wait_timeout"):
         assert n in names
 
 
@@ -45,8 +46,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_strerror_names_every_code(lib):
-    for code in range(0, -12, -1):
-        assert lib.based_strerror(code).decode() != "unknown error code"
+    for code in range(0, -13, -1):
+        name = lib.based_fwd_strerror(code).decode()
+        assert name != "unknown error code"
+        assert lib.based_strerror(code).decode() == name  # the older name is the same function
+    assert lib.based_fwd_strerror(-99).decode() == "unknown error code"
     assert lib.based_strerror(-99).decode() == "unknown error code"
     assert lib.based_abi_version() == 10100
 
