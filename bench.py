@@ -394,7 +394,12 @@ def run_gpu(args, w, world, rank, local):
                      "kernel": "based_fwd_kernel", "kernel_ms": fwd_avg_ms,
                      "kernel_timing": "CUDA events around the forward kernel on its launch stream, "
                                       "K steps after the timed region, launched without overlap",
-                     "algorithmic_bytes": wbytes, "peak_source": f"{peak_kind} (hbm_gbs)"},
+                     "algorithmic_bytes": wbytes, "peak_source": f"{peak_kind} (hbm_gbs)",
+                     # the whole call (every kernel of the step) against the same bound
+                     "call_achieved": wbytes / (ms_per_step * 1e-3) / 1e9,
+                     "call_frac": wbytes / (ms_per_step * 1e-3) / 1e9 / hbm,
+                     "call_roofline_ms": t_roof_ms,
+                     "kernel_source_sha": kernel_source_sha()},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
         "e2e": e2e,
