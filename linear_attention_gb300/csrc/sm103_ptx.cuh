@@ -33,11 +33,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-// Invalidates an mbarrier whose phases are all complete, so that its memory may be used for
-// something else (the fused kernel's second phase reuses the first phase's shared memory).
-__device__ __forceinline__ void mbar_inval(uint32_t bar) {
-    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 // Non-blocking test of a phase (no suspension): true if the phase with this parity has completed.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -242,11 +237,6 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
         "r"(r[15])
         : "memory");
 }
-__device__ __forceinline__ void tmem_st_x2(uint32_t taddr, uint32_t a, uint32_t b) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a),
-                 "r"(b)
-                 : "memory");
-}
 __device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t a) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
 }
@@ -306,34 +296,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return r;
-}
-
-// ------------------------------------------------------------------------------------------------
-// Global-memory flags between CTAs of one grid (gpu scope)
-// ------------------------------------------------------------------------------------------------
-// Adds v with release semantics: every write this thread made before (and, through a preceding
-// fence and barrier, the writes of the threads it synchronised with) is visible to a thread that
-// observes the new value with an acquire load.
-__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-// Adds v with acquire-release semantics and returns the old value.
-__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t *p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-// Streaming 16-byte global store (the output is written once and not re-read).
-__device__ __forceinline__ void st_global_cs_v4(void *p, float a, float b, float c, float d) {
-    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
 }
 
 }  // namespace based
