@@ -157,6 +157,31 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~stat
     return p;
 }
 
+// The kernels index the slots with the plan's tables and check none of them on the device: every
+// prefix must read only slots the aggregate pass writes, every piece must lie in its lane's
+// chunks, and every scan run must stay within the slots. A plan that breaks this is a library
+// bug; the call then fails before anything is launched (the partition check in the tests
+// exercises the same invariants over many shapes).
+bool plan_in_bounds(const Plan &p) {
+    if (!p.need_agg) return true;
+    const AggPieces &A = p.agg.pieces;
+    if (A.n < 1 || A.n > kMaxPieces || A.n_cta < 1 || A.n_cta > p.G) return false;
+    if (A.cta_first[0] != 0 || A.cta_first[A.n_cta] != A.n) return false;
+    for (int j = 0; j < A.n_cta; ++j)
+        if (A.cta_first[j + 1] < A.cta_first[j]) return false;
+    for (int q = 0; q < A.n; ++q)
+        if (A.len[q] < 1 || A.g0[q] < 0 || static_cast<long long>(A.g0[q]) + A.len[q] > p.N) return false;
+    for (int r = 0; r < p.G; ++r) {
+        const int cnt = p.agg.pre.cnt[r];
+        if (cnt == 0) continue;
+        if (cnt > (p.agg.scan ? 1 : kMaxChain) || p.agg.pre.slot[r] + cnt > A.n) return false;
+    }
+    if (p.agg.scan)
+        for (int i = 0; i < p.agg.runs.n; ++i)
+            if (p.agg.runs.len[i] < 2 || p.agg.runs.start[i] + p.agg.runs.len[i] > A.n) return false;
+    return true;
+}
+
 // out_elem: bytes per output element (4 for fp32, 2 for bf16)
 int check_args(const void *q, const void *k, const void *v, int B, int T, int H, int K, int V,
                const void *o, size_t out_elem = 4) {
@@ -268,6 +293,10 @@ int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, i
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
     DeviceState &d = g_dev[dev];
     const Plan p = make_plan(B, T, H, K, V, d.sms, max_ws);
+    if (!plan_in_bounds(p)) {
+        snprintf(tl_cuda_error, sizeof(tl_cuda_error), "internal error: work plan out of bounds");
+        return BASED_ERR_BAD_ARGUMENT;
+    }
     if (!(scale > 0.0f) || std::isnan(scale)) scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(K)));
     if (own_ws) {
         std::lock_guard<std::mutex> lk(d.m);
