@@ -260,9 +260,10 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     if (p.need_agg) {
         // 512 threads (dedicated slot writers) when a CTA sums several pieces, else 384
         const int threads = p.agg.pieces.n > p.agg.pieces.n_cta ? kAggThreads : 384;
-        based_agg_kernel<K, V><<<p.agg.pieces.n_cta * p.L, threads, CF::SMEM_AGG, st>>>(mk, mv, ws, H, p.n_c, p.L,
-                                                                                    p.agg.pieces);
-        BASED_CUDA(cudaGetLastError());
+        // a programmatic dependent of the previous kernel in the stream (it waits for that kernel
+        // before its first access to memory), unless the caller brackets the call with events
+        BASED_CUDA(launch_dependent(based_agg_kernel<K, V>, dim3(p.agg.pieces.n_cta * p.L), dim3(threads),
+                                    CF::SMEM_AGG, st, !ev_begin, mk, mv, ws, H, p.n_c, p.L, p.agg.pieces));
         if (p.agg.scan) {  // otherwise each forward CTA sums the (at most kMaxChain) slots it needs
             dim3 grid((p.slot_floats / 4 + 255) / 256, p.agg.runs.n * p.L);
             BASED_CUDA(launch_dependent(based_scan_kernel, grid, dim3(256), 0, st, true, ws,
@@ -270,14 +271,15 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
         }
     }
     if (ev_begin) BASED_CUDA(cudaEventRecord(ev_begin, st));
-    // A forward kernel that follows the aggregate pass is launched as its programmatic dependent
-    // (it starts while that pass finishes; only its read of the prefix slots waits). Without the
-    // aggregate pass, or when the caller brackets it with events, it is an ordinary launch: it
-    // must not start before earlier work in the stream that may produce q, k or v.
-    const bool dependent = p.need_agg && !ev_begin;
+    // The forward kernel is launched as a programmatic dependent of the kernel before it: after
+    // the aggregate pass it starts while that pass finishes (only its read of the prefix slots
+    // waits for it); as the first kernel of the call it waits for the previous kernel of the stream
+    // before its first access to memory. When the caller brackets the call with events, every
+    // kernel is an ordinary launch.
+    const bool dependent = !ev_begin;
     BASED_CUDA(launch_dependent(based_fwd_kernel<K, V, OBF>, dim3(p.G * p.L), dim3(kFwdThreads), CF::SMEM_FWD, st,
                                 dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
-                                p.N, p.G, p.L, p.agg.pieces.n, scale, p.agg.pre));
+                                p.N, p.G, p.L, p.agg.pieces.n, scale, p.agg.pre, p.need_agg ? 0 : 1));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }

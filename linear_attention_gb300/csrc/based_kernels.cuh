@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G, int L,
-                 int lane_slots, float scale, const __grid_constant__ Prefixes pre) {
+                 int lane_slots, float scale, const __grid_constant__ Prefixes pre, int wait_prev) {
     using CF = Cfg<K, V>;
     constexpr bool FAST = CF::FAST;
     extern __shared__ uint8_t smem_raw[];
@@ -756,6 +756,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_o);
+        // The first kernel of a call is launched as a programmatic dependent of the previous
+        // kernel in the stream (whose outputs may be q, k or v, and which may still read o):
+        // nothing of this grid touches global memory before this thread's first loads, and those
+        // wait for that kernel. After an aggregate pass the previous call has already completed.
+        if (wait_prev) griddep_wait();
         Cursor cu;
         cu.init(g0, nchunks, n_c, Hl, L, r_lane);
         for (int n = 0; n < n_early; ++n, cu.next()) issue_loads(n, cu);
@@ -788,6 +793,9 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     if (threadIdx.x == 0) BASED_TRACE_EV(63, 21);  // set-up done
+    // the next call's first kernel may start launching now; it waits for this grid before it
+    // touches memory
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ================================ TMA producer =========================================
@@ -1495,9 +1503,6 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     constexpr int S = CF::A_NST;
     constexpr int NP = CF::A_NPHIK;
     using AB = AggBar<S, NP>;
-    // the scan / forward kernel may start launching now; it waits for this grid before it
-    // reads the slots
-    griddep_launch_dependents();
     constexpr int AB_TMA_FULL0 = AB::TMA_FULL0, AB_STAGE_FREE0 = AB::STAGE_FREE0,
                   AB_PHIK_FULL0 = AB::PHIK_FULL0, AB_PHIK_FREE0 = AB::PHIK_FREE0,
                   AB_AGG_DONE0 = AB::AGG_DONE0, AB_SLOT_READ0 = AB::SLOT_READ0, AB_DRAIN = AB::DRAIN,
@@ -1553,6 +1558,10 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         // the first loads go out now (this thread is the TMA producer)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
+        // launched as a programmatic dependent of the previous kernel in the stream (whose
+        // outputs may be k or v, and which may still read the slots): nothing of this grid touches
+        // global memory before this thread's first loads, and those wait for that kernel
+        griddep_wait();
         PieceWalk w;
         w.init(ap, p0, p1, n_c, Hl, L, r_lane);
         for (int u = 0; u < n_early; ++u, w.next()) issue_loads(u, w.cu);
@@ -1575,6 +1584,9 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the scan / forward kernel may start launching now (the previous kernel has completed): it
+    // waits for this grid before it reads the slots
+    griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
