@@ -87,10 +87,12 @@ struct Plan {
     int L;          // head lanes (choose_lanes); every lane has the same partition and plan
     long long N;    // chunks of one lane
     int G;          // ranges of one lane (forward CTAs: G L)
-    bool need_agg;  // some range ends inside a head
+    bool lead_in;   // ranges that start inside a head run a lead-in (else: slots, see Ranges)
+    bool need_agg;  // the aggregate pass runs (slots, and some range ends inside a head)
     int slot_floats;
     size_t ws_bytes;
     AggPlan agg;    // pieces of the aggregate pass, the forward CTAs' prefixes, the scan runs
+    Ranges rg;      // the forward CTAs' ranges and how each gets its prefix
 };
 
 constexpr int kMaxDevices = 64;
@@ -153,17 +155,45 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~stat
     const size_t slot_bytes = static_cast<size_t>(p.slot_floats) * sizeof(float);
     const size_t max_slots = max_ws / slot_bytes / p.L;  // per lane
     make_agg_plan(p.N, p.G, p.n_c, p.G, max_slots < kMaxPieces ? static_cast<int>(max_slots) : kMaxPieces, p.agg);
+    p.lead_in = false;
+    if (p.need_agg) {
+        // lead-ins instead of slots, where the cost model finds them faster
+        const int used = choose_lead_in(p.N, p.G, p.n_c, V, p.agg, p.rg);
+        if (used > 0) {
+            p.lead_in = true;
+            p.need_agg = false;
+            p.G = used;  // the ranges past the last are empty: no CTAs for them
+        }
+    }
+    if (!p.lead_in) {
+        for (int j = 0; j <= p.G; ++j) p.rg.g0[j] = static_cast<int32_t>(cta_range(p.N, p.G, j).g0);  // j = G: N
+        p.rg.lead_in = 0;
+        for (int j = 0; j < p.G; ++j) {
+            p.rg.slot[j] = p.agg.pre.slot[j];
+            p.rg.cnt[j] = p.agg.pre.cnt[j];
+        }
+    }
     p.ws_bytes = p.need_agg ? static_cast<size_t>(p.L) * p.agg.pieces.n * slot_bytes : 0;
     return p;
 }
 
-// The kernels index the slots with the plan's tables and check none of them on the device: every
+// The kernels index the slots with the plan's tables and check none of them on the device: the
+// ranges must cut the lane's chunks in order, each lead-in must stay inside its head, every
 // prefix must read only slots the aggregate pass writes, every piece must lie in its lane's
 // chunks, and every scan run must stay within the slots. A plan that breaks this is a library
 // bug; the call then fails before anything is launched (the partition check in the tests
 // exercises the same invariants over many shapes).
 bool plan_in_bounds(const Plan &p) {
+    if (p.G < 1 || p.G > kMaxRanges || p.rg.g0[0] != 0 || p.rg.g0[p.G] != p.N) return false;
+    if (p.rg.lead_in != (p.lead_in ? 1 : 0)) return false;
+    for (int j = 0; j < p.G; ++j) {
+        if (p.rg.g0[j + 1] <= p.rg.g0[j]) return false;
+        if (p.lead_in && p.rg.cnt[j] != 0) return false;
+        if (!p.need_agg && p.rg.cnt[j] != 0) return false;
+    }
     if (!p.need_agg) return true;
+    for (int j = 0; j < p.G; ++j)
+        if (p.rg.cnt[j] != p.agg.pre.cnt[j] || p.rg.slot[j] != p.agg.pre.slot[j]) return false;
     const AggPieces &A = p.agg.pieces;
     if (A.n < 1 || A.n > kMaxPieces || A.n_cta < 1 || A.n_cta > p.G) return false;
     if (A.cta_first[0] != 0 || A.cta_first[A.n_cta] != A.n) return false;
@@ -227,12 +257,17 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
            float scale, void *o, float *ws, const Plan &p, DeviceState &d, cudaStream_t st,
            cudaEvent_t ev_begin, cudaEvent_t ev_end) {
     using CF = Cfg<K, V>;
+    // the forward kernel's instances: prefixes from slots, and lead-ins (V = 64; for V = 128 the
+    // same instance)
+    void (*const fwd_slots)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, const float *, int, int, int,
+                            long long, int, int, int, float, Ranges, int) = based_fwd_kernel<K, V, OBF, false>;
+    decltype(fwd_slots) fwd_lead = based_fwd_kernel<K, V, OBF, CF::FAST>;
     {
         std::lock_guard<std::mutex> lk(d.m);
         bool &done = d.attrs_done[K == 16][V == 128][OBF];
         if (!done) {
-            BASED_CUDA(cudaFuncSetAttribute(based_fwd_kernel<K, V, OBF>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_FWD));
+            BASED_CUDA(cudaFuncSetAttribute(fwd_slots, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_FWD));
+            BASED_CUDA(cudaFuncSetAttribute(fwd_lead, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_FWD));
             BASED_CUDA(cudaFuncSetAttribute(based_agg_kernel<K, V>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_AGG));
             done = true;
@@ -277,9 +312,9 @@ int launch(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T
     // before its first access to memory. When the caller brackets the call with events, every
     // kernel is an ordinary launch.
     const bool dependent = !ev_begin;
-    BASED_CUDA(launch_dependent(based_fwd_kernel<K, V, OBF>, dim3(p.G * p.L), dim3(kFwdThreads), CF::SMEM_FWD, st,
+    BASED_CUDA(launch_dependent(p.lead_in ? fwd_lead : fwd_slots, dim3(p.G * p.L), dim3(kFwdThreads), CF::SMEM_FWD, st,
                                 dependent, mq, mk, mv, mo, static_cast<const float *>(ws), T, H, p.n_c,
-                                p.N, p.G, p.L, p.agg.pieces.n, scale, p.agg.pre, p.need_agg ? 0 : 1));
+                                p.N, p.G, p.L, p.agg.pieces.n, scale, p.rg, p.need_agg ? 0 : 1));
     if (ev_end) BASED_CUDA(cudaEventRecord(ev_end, st));
     return BASED_OK;
 }

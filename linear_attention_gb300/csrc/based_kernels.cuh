@@ -56,7 +56,8 @@ enum TraceEvent {
     TE_TMA_ISSUE = 0, TE_A_READY, TE_AV_ISSUED, TE_QK_ISSUED, TE_UPD_ISSUED, TE_RO_ISSUED,
     TE_POLY_BEGIN, TE_POLY_END, TE_PHIK_BEGIN, TE_PHIK_END, TE_PHIQ_BEGIN, TE_PHIQ_END,
     TE_EPI_BEGIN, TE_EPI_OFREE, TE_EPI_END, TE_CONV_BEGIN, TE_CONV_READ, TE_CONV_END,
-    TE_POLY_LD0, TE_POLY_ST0, TE_POLY_LD1, TE_POLY_ST1
+    TE_POLY_LD0, TE_POLY_ST0, TE_POLY_LD1, TE_POLY_ST1,
+    TE_LEAD_ISSUE = 23, TE_LEAD_BUILD0, TE_LEAD_BUILD1, TE_LEAD_UPD  // lead-in chunk i at index i
 };
 
 enum WaitSite : uint32_t {
@@ -154,7 +155,9 @@ struct Cfg {
     static constexpr int OFF_RAWQ = 0;
     static constexpr int OFF_RAWK = OFF_RAWQ + NST * RAW;
     static constexpr int OFF_V = OFF_RAWK + NST * RAW;
-    // ones block: one 16-token k-step of an MN-major SW128 atom (2 KB), re-used by every k-step
+    // ones block: one 16-token k-step of an MN-major SW128 atom (2 KB), re-used by every k-step.
+    // A v tile reaches it with a positive leading-byte offset: the stages' v tiles the one right
+    // after them, the lead-in stages' v tiles a copy at the end of shared memory.
     static constexpr int ONES = ZROW ? 2048 : 0;
     static constexpr int OFF_ONES = OFF_V + NST * VT;
     static constexpr int OFF_PHIK = OFF_ONES + ONES;
@@ -171,7 +174,22 @@ struct Cfg {
     static constexpr int EPI_ROWS = NOST == 1 ? 32 : 128;
     static constexpr int OFF_OST = OFF_ZONES + 1024;
     static constexpr int OFF_BAR = OFF_OST + NOST * OST;
-    static constexpr int SMEM_FWD = OFF_BAR + 256 + 1024;  // + alignment slack
+    // Lead-in stages (V = 64): k and v tiles of NLS lead-in chunks in flight. They use memory
+    // that the range's chunks first need after the lead-in: for K = 16 the state operand buffers
+    // (stages 0, 1) and the output staging (stage 2); for K = 8, whose state operands are small,
+    // a region of their own (stages 0, 1) and the output staging (stage 2).
+    static constexpr int NLS = FAST ? 3 : 0;
+    static constexpr int OFF_LEAD = align_up(OFF_BAR + 256, 1024);
+    static constexpr int LEAD_OWN = (FAST && K == 8) ? 2 * (VT + RAW) : 0;
+    static constexpr int LEAD_BASE = K == 16 ? OFF_SBF : OFF_LEAD;
+    __host__ __device__ static constexpr int lead_v(int i) { return i < 2 ? LEAD_BASE + i * VT : OFF_OST; }
+    __host__ __device__ static constexpr int lead_k(int i) {
+        return i < 2 ? LEAD_BASE + 2 * VT + i * RAW : OFF_OST + VT;
+    }
+    static_assert(!FAST || K != 16 || 2 * (VT + RAW) <= NSBF * SBF, "lead-in stages over the state operands");
+    static_assert(!FAST || VT + RAW <= NOST * OST, "lead-in stage over the output staging");
+    static constexpr int OFF_LONES = align_up(OFF_LEAD + LEAD_OWN, 1024);
+    static constexpr int SMEM_FWD = OFF_LONES + (FAST ? ONES : 0) + 1024;  // + alignment slack
     // The z MMA reads 8 feature blocks (32 KB) from the phi(k) tile start; they must be inside
     // the allocation even when the tile has fewer blocks (their rows of D are never read).
     static_assert(ZROW || OFF_PHIK + 8 * 4096 <= OFF_BAR, "z MMA window leaves shared memory");
@@ -636,6 +654,72 @@ inline void make_agg_plan(long long N, int G, int n_c, int max_cta, int max_slot
     if (100 * cost_bal < 85 * cost_one) P = B;
 }
 
+// ------------------------------------------------------------------------------------------------
+// Forward CTAs' ranges (host plan, read by the forward kernel). Range j of a lane is its chunks
+// [g0[j], g0[j + 1]). A range that starts inside a head continues the state of that head's chunks
+// before it, which it gets in one of two ways, the same for every range of a call:
+//  - from slots: the aggregate pass wrote partial states, and the CTA sums slots slot[j] ..
+//    slot[j] + cnt[j] - 1 (cnt = 0 at a head start); the chunks are cut evenly (cta_range);
+//  - by a lead-in (V = 64, lead_in set): the CTA first runs the state update alone over the
+//    g0[j] % n_c chunks of its head before g0[j], so that the call is the forward kernel alone;
+//    the cut then gives each range as many chunks as its lead-in leaves room for (lead_cut).
+// ------------------------------------------------------------------------------------------------
+struct Ranges {
+    int32_t g0[kMaxRanges + 1];
+    uint16_t slot[kMaxRanges];
+    uint8_t cnt[kMaxRanges];
+    int32_t lead_in;
+};
+
+// Cost model of a CTA, in thousandths of the time of one chunk of the forward pipeline (fitted to
+// stage traces of whole calls on GB300, V = 64, K = 16; one chunk is about 1.77 us):
+// kStartCost for its start and end (set-up, the first loads, the pipeline's fill and drain),
+// kLeadStart more when it has a lead-in, kLeadCost per lead-in chunk (the f(k) tile and the state
+// update alone), 1000 per chunk of its range.
+constexpr long long kStartCost = 4950, kLeadStart = 815, kLeadCost = 252;
+__host__ __device__ inline long long range_cost(long long lead, long long len) {
+    return kStartCost + (lead > 0 ? kLeadStart + lead * kLeadCost : 0) + 1000 * len;
+}
+
+// Lead-in cut of a lane's N chunks (n_c per head) into at most G ranges: the smallest makespan M
+// (cost model above) for which the greedy cut, in which each range takes every chunk that M
+// leaves room for after its lead-in, covers all N chunks. Writes the cut to R.g0 (ranges past
+// the last are empty, g0 = N), sets R.lead_in, clears R.cnt, and returns M. A greedy range that
+// ends further into a head leaves the next range less room, by less than it gained (kLeadCost <
+// 1000) except when it leaves a head start (kLeadStart), so coverage grows with M nearly
+// everywhere: the bisection finds the smallest M up to such steps, and the cut it returns always
+// covers the chunks with every range within M.
+inline long long lead_cut(long long N, int G, int n_c, Ranges &R) {
+    auto greedy = [&](long long M, bool write) -> bool {
+        long long g = 0;
+        int j = 0;
+        for (; j < G && g < N; ++j) {
+            const long long s = g % n_c;
+            const long long room = (M - range_cost(s, 0)) / 1000;
+            if (room < 1) return false;
+            if (write) R.g0[j] = static_cast<int32_t>(g);
+            g = g + room < N ? g + room : N;
+        }
+        if (g < N) return false;
+        if (write)
+            for (; j <= G; ++j) R.g0[j] = static_cast<int32_t>(N);
+        return true;
+    };
+    long long lo = 0, hi = range_cost(0, N);  // hi: the first range takes everything
+    while (hi - lo > 1) {
+        const long long mid = lo + (hi - lo) / 2;
+        if (greedy(mid, false)) hi = mid;
+        else lo = mid;
+    }
+    greedy(hi, true);
+    R.lead_in = 1;
+    for (int j = 0; j < G; ++j) {
+        R.slot[j] = 0;
+        R.cnt[j] = 0;
+    }
+    return hi;
+}
+
 // Walks the chunks of a range without divisions: (b, h, c) advance like an odometer.
 // g is a chunk index of one head lane (see choose_lanes): lane r's heads are h = hv L + r,
 // hv < Hl = H / L.
@@ -684,19 +768,23 @@ struct Cursor {
 enum FwdBar {
     FB_TMA_FULL0 = 0, FB_STAGE_FREE0 = 3, FB_S_FULL = 6, FB_A_FULL, FB_O_FULL0, FB_O_FULL1,
     FB_O_FREE0, FB_O_FREE1, FB_AV_DONE, FB_PHIQ_FULL, FB_PHIQ_FREE, FB_PHIK_FULL, FB_PHIK_FREE,
-    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_DRAIN_B, FB_AV_DONE1, FB_SBF_FULL1, FB_COUNT
+    FB_UPD_DONE, FB_CONV_READ, FB_SBF_FULL, FB_DRAIN, FB_DRAIN_B, FB_AV_DONE1, FB_SBF_FULL1,
+    FB_LFULL0, FB_LFREE0 = FB_LFULL0 + 3, FB_COUNT = FB_LFREE0 + 3  // lead-in stages (NLS <= 3)
 };
 
 // OBF: the output tile is written as bf16 (round to nearest even from the fp32 quotient) instead
-// of fp32.
-template <int K, int V, bool OBF>
+// of fp32. LEADIN: the ranges that start inside a head run lead-ins (else they load their prefix
+// from slots); each instance carries only its own way, which keeps the hot code of the other
+// roles small.
+template <int K, int V, bool OBF, bool LEADIN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const float *__restrict__ prefix, int T, int H, int n_c, long long N, int G, int L,
-                 int lane_slots, float scale, const __grid_constant__ Prefixes pre, int wait_prev) {
+                 int lane_slots, float scale, const __grid_constant__ Ranges rg, int wait_prev) {
     using CF = Cfg<K, V>;
     constexpr bool FAST = CF::FAST;
+    static_assert(!LEADIN || FAST, "lead-ins are built for V = 64");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -715,10 +803,17 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // range j of head lane r (N, G: chunks and ranges of one lane; lane_slots: slots per lane)
     const int j_range = static_cast<int>(blockIdx.x) / L, r_lane = static_cast<int>(blockIdx.x) % L;
     const int Hl = H / L;
-    const Part part = cta_range(N, G, j_range);
-    const long long g0 = part.g0, g1 = part.g1;
+    const long long g0 = rg.g0[j_range], g1 = rg.g0[j_range + 1];
     const int nchunks = static_cast<int>(g1 - g0);
     if (nchunks <= 0) return;
+    // Lead-in (V = 64): the chunks of the first head before g0, whose state update alone runs
+    // first. Lead-in chunk i is loaded into lead-in stage i % NLS (k and v only), chunk n of the
+    // range into stage n % NST.
+    const int n_lead = LEADIN ? static_cast<int>(g0 % n_c) : 0;
+    constexpr int NLS = CF::NLS > 0 ? CF::NLS : 1;
+    constexpr bool kLeadOverSbf = LEADIN && K == 16;  // lead-in stages over the state operands
+    auto stage_of = [&](int n) -> int { return n % CF::NST; };
+    auto stage_par = [&](int n) -> uint32_t { return static_cast<uint32_t>((n / CF::NST) & 1); };
     BASED_TRACE_INIT;
     if (threadIdx.x == 0) BASED_TRACE_EV(63, 20);  // CTA start
 #ifdef BASED_TRACE
@@ -726,6 +821,16 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 22] = global_timer_ns();
 #endif
 
+    // k, v tiles of lead-in chunk i (cursor position cu) into lead-in stage i % NLS, completing on
+    // LFULL
+    auto issue_lead = [&](int i, const Cursor &cu) {
+        const int ls = i % NLS;
+        const uint32_t bar = BAR(FB_LFULL0 + ls);
+        BASED_TRACE_EV(i, TE_LEAD_ISSUE);
+        mbar_arrive_expect_tx(bar, CF::RAW + CF::VT);
+        tma_load_4d(sb + CF::lead_k(ls), &tm_k, bar, 0, cu.h, cu.t0(), cu.b);
+        tma_load_4d(sb + CF::lead_v(ls), &tm_v, bar, 0, cu.h, cu.t0(), cu.b);
+    };
     // q, k, v tiles of chunk n (cursor position cu) into stage n % NST, completing on TMA_FULL
     auto issue_loads = [&](int n, const Cursor &cu) {
         const int s = n % CF::NST;
@@ -739,6 +844,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_load_4d(sb + CF::OFF_V + s * CF::VT + 16384, &tm_v, bar, 64, cu.h, cu.t0(), cu.b);
     };
     const int n_early = nchunks < CF::NST ? nchunks : CF::NST;  // loads issued during set-up
+    const int n_lead_early = n_lead < NLS ? n_lead : NLS;
 
     // ---- set-up: barriers, constant tiles, TMEM -------------------------------------------------
     if (threadIdx.x == 0) {
@@ -746,7 +852,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // STAGE_FREE: one commit from each MMA issuer. V = 64: six warps compute the Taylor
         // weights and three convert the state (see the role split below).
         constexpr uint32_t NW = FAST ? 6 : 4, NC = FAST ? 3 : 4;
-        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, NW, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, NC, NC, 1, 1, 1, NC};
+        const uint32_t counts[FB_COUNT] = {1, 1, 1, 2, 2, 2, 1, NW, 1, 1, 4, 4, 1, 4, 1, 4, 1, 1, NC, NC, 1, 1, 1, NC,
+                                           1, 1, 1, 1, 1, 1};
         for (int i = 0; i < FB_COUNT; ++i) mbar_init(BAR(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -761,22 +868,37 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // nothing of this grid touches global memory before this thread's first loads, and those
         // wait for that kernel. After an aggregate pass the previous call has already completed.
         if (wait_prev) griddep_wait();
+        if (LEADIN && n_lead > 0) {
+            // the lead-in's first loads, then the next NLS lead-in chunks into L2 (each later load
+            // prefetches the chunk NLS after it), so that the lead-in's loads wait on L2 rather
+            // than DRAM
+            Cursor cl;
+            cl.init(g0 - n_lead, n_lead, n_c, Hl, L, r_lane);
+            for (int i = 0; i < n_lead_early; ++i, cl.next()) issue_lead(i, cl);
+            for (int i = n_lead_early; i < n_lead && i < 2 * NLS; ++i, cl.next()) {
+                tma_prefetch_4d(&tm_k, 0, cl.h, cl.t0(), cl.b);
+                tma_prefetch_4d(&tm_v, 0, cl.h, cl.t0(), cl.b);
+            }
+        }
         Cursor cu;
         cu.init(g0, nchunks, n_c, Hl, L, r_lane);
         for (int n = 0; n < n_early; ++n, cu.next()) issue_loads(n, cu);
     }
     // bf16 state operands: zero once (rows V+2.. stay zero; rows 0..V+1 are rewritten per use).
-    for (int i = threadIdx.x; i < CF::NSBF * CF::SBF / 16; i += kFwdThreads)
-        st_shared_v4(sb + CF::OFF_SBF + 16u * i, 0u, 0u, 0u, 0u);
+    // Lead-in stages over them: the conversion warps zero rows V+2.. after the lead-in instead.
+    if (!(kLeadOverSbf && n_lead > 0))
+        for (int i = threadIdx.x; i < CF::NSBF * CF::SBF / 16; i += kFwdThreads)
+            st_shared_v4(sb + CF::OFF_SBF + 16u * i, 0u, 0u, 0u, 0u);
     if constexpr (CF::ZROW) {
         // ones block: an MN-major SW128 block whose element 0 is 1.0 in every token row. It is
         // the extra operand block behind v_c: A rows 64..127 of the state update (so that row 64
         // of S^T accumulates z) and B columns 64..79 of A [v | 1] (column 64 = rowsum A).
-        for (int i = threadIdx.x; i < CF::ONES / 16; i += kFwdThreads)
-            st_shared_v4(sb + CF::OFF_ONES + 16u * i, 0u, 0u, 0u, 0u);
+        for (int i = threadIdx.x; i < 2 * CF::ONES / 16; i += kFwdThreads)
+            st_shared_v4(sb + (i < CF::ONES / 16 ? CF::OFF_ONES : CF::OFF_LONES - CF::ONES) + 16u * i, 0u, 0u, 0u,
+                         0u);
         __syncthreads();
-        if (threadIdx.x < 16)
-            st_shared_u16(sb + CF::OFF_ONES + sw128(threadIdx.x, 0), 0x3F80);
+        if (threadIdx.x < 32)
+            st_shared_u16(sb + (threadIdx.x < 16 ? CF::OFF_ONES : CF::OFF_LONES) + sw128(threadIdx.x & 15, 0), 0x3F80);
     }
     // ones column as a K-major SW32 operand: N row 0 = 16 ones, rows 1..15 = 0.
     if (threadIdx.x < 32)
@@ -800,11 +922,31 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == 0) {
         // ================================ TMA producer =========================================
         if (lane == 0) {
-            int issued = n_early;
+            int lead_issued = n_lead_early, issued = n_early;
+            bool ok = true;
+            if (LEADIN && n_lead > n_lead_early) {
+                Cursor cl, cp;  // cp: NLS chunks ahead (L2 prefetch)
+                cl.init(g0 - n_lead, n_lead, n_c, Hl, L, r_lane);
+                cp.init(g0 - n_lead, n_lead, n_c, Hl, L, r_lane);
+                for (int i = 0; i < n_lead_early; ++i) cl.next();
+                for (int i = 0; i < 2 * NLS; ++i) cp.next();
+                for (int i = n_lead_early; i < n_lead; ++i, cl.next()) {
+                    const int ls = i % NLS;
+                    if (!(ok = wait_bar(BAR(FB_LFREE0 + ls), ((i / NLS) - 1) & 1, abort_flag, SITE_STAGE_FREE)))
+                        break;
+                    issue_lead(i, cl);
+                    ++lead_issued;
+                    if (i + NLS >= 2 * NLS && i + NLS < n_lead) {
+                        tma_prefetch_4d(&tm_k, 0, cp.h, cp.t0(), cp.b);
+                        tma_prefetch_4d(&tm_v, 0, cp.h, cp.t0(), cp.b);
+                        cp.next();
+                    }
+                }
+            }
             Cursor cu;
             cu.init(g0, nchunks, n_c, Hl, L, r_lane);
             for (int n = 0; n < n_early; ++n) cu.next();
-            for (int n = n_early; n < nchunks; ++n, cu.next()) {
+            for (int n = n_early; ok && n < nchunks; ++n, cu.next()) {
                 const int s = n % CF::NST;
                 if (!wait_bar(BAR(FB_STAGE_FREE0 + s), ((n / CF::NST) - 1) & 1, abort_flag,
                               SITE_STAGE_FREE))
@@ -817,6 +959,9 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (m >= 0)
                         wait_bar(BAR(FB_TMA_FULL0 + m % CF::NST), (m / CF::NST) & 1, nullptr,
                                  SITE_DRAIN, kDrainLimitNs);
+                for (int m = lead_issued - NLS; m < lead_issued; ++m)
+                    if (m >= 0)
+                        wait_bar(BAR(FB_LFULL0 + m % NLS), (m / NLS) & 1, nullptr, SITE_DRAIN, kDrainLimitNs);
             }
         }
     } else if (warp == 1 || warp == 3) {
@@ -851,8 +996,8 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint64_t d_k = smem_desc(sb + CF::OFF_RAWK, 16, 256, LAYOUT_SW32);
                 // s = q k^T of chunk m into the scores tile, completing on S_FULL
                 auto issue_qk = [&](int m) -> bool {
-                    const int sm = m % CF::NST;
-                    if (!wait_bar(BAR(FB_TMA_FULL0 + sm), (m / CF::NST) & 1, abort_flag, SITE_TMA_FULL))
+                    const int sm = stage_of(m);
+                    if (!wait_bar(BAR(FB_TMA_FULL0 + sm), stage_par(m), abort_flag, SITE_TMA_FULL))
                         return false;
                     tc_fence_after();
                     mma_ss(t_sc, dadd(d_q, sm * CF::RAW), dadd(d_k, sm * CF::RAW), ID_QK, 0);
@@ -861,7 +1006,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 };
                 bool ok = issue_qk(0);
                 for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
-                    const int s = n % CF::NST;
+                    const int s = stage_of(n);
                     const int ob = FAST ? (n & 1) : 0;
                     const uint64_t d_va = s == 0 ? d_va0 : (s == 1 ? d_va1 : d_va2);
                     const uint32_t t_out = ob ? t_o1 : t_o0;
@@ -873,7 +1018,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     bool qk_next = false;
                     if constexpr (FAST) {
                         const int m = n + 1;
-                        if (m < nchunks && mbar_test_wait(BAR(FB_TMA_FULL0 + m % CF::NST), (m / CF::NST) & 1)) {
+                        if (m < nchunks && mbar_test_wait(BAR(FB_TMA_FULL0 + stage_of(m)), stage_par(m))) {
                             if (!(ok = issue_qk(m))) break;
                             qk_next = true;
                             BASED_TRACE_EV(n, TE_QK_ISSUED);
@@ -921,14 +1066,16 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const uint64_t d_sbf1 = smem_desc(sb + CF::OFF_SBF + (CF::NSBF - 1) * CF::SBF, 16, 256, LAYOUT_SW32);
                 const uint64_t d_phik = smem_desc(sb + CF::OFF_PHIK, 4096, 256, LAYOUT_SW32);
                 const uint64_t d_phiq = smem_desc(sb + CF::OFF_PHIQ, 16, 256, LAYOUT_SW32);
-                int ro_idx = 0, upd_idx = 0;
+                // ro_idx: read-outs (= conversions consumed); upd_idx, qn: fills of the f(k) and
+                // the f~(q) tile consumed
+                int ro_idx = 0, upd_idx = 0, qn = 0;
                 bool ok = true;
                 // release_stage >= 0: that stage is released as soon as f~(q_c) is built (the
                 // builders have read its raw tiles; the commit tracks the state update issued
                 // before, which read v_c)
                 auto issue_ro = [&](int n, uint32_t t_out, int release_stage) -> bool {
                     // O += f~(q_c) [S | z_hi z_lo], after O = A [v_c | 1] has completed
-                    if (!wait_bar(BAR(FB_PHIQ_FULL), ro_idx & 1, abort_flag, SITE_PHIQ_FULL)) return false;
+                    if (!wait_bar(BAR(FB_PHIQ_FULL), qn & 1, abort_flag, SITE_PHIQ_FULL)) return false;
                     if (release_stage >= 0) mma_commit(BAR(FB_STAGE_FREE0 + release_stage));
                     // conversion ro_idx (one SBF_FULL barrier per state operand buffer)
                     if (!wait_bar(BAR(sbf_full_bar(ro_idx)), sbf_full_par(ro_idx), abort_flag, SITE_SBF_FULL))
@@ -944,6 +1091,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mma_ss(t_out, dadd(d_phiq, 4096 * f), dadd(db, CF::SBF_BLK * f), ID_RO, 1);
                     mma_commit(BAR(FB_PHIQ_FREE));
                     ++ro_idx;
+                    ++qn;
                     return true;
                 };
                 auto issue_upd = [&](int n, uint64_t d_va) -> bool {
@@ -971,8 +1119,36 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ++upd_idx;
                     return true;
                 };
+                if constexpr (LEADIN) {
+                    // Lead-in: S^T += [v_c | 1]^T f(k_c) over the head's chunks before the range.
+                    // Their f(k) tiles alternate between the f(k) and the f~(q) tile, so that the
+                    // next one is built while this one is summed. One UPD_DONE phase marks the
+                    // whole lead-in for the conversion.
+                    const uint64_t d_phiq_k = smem_desc(sb + CF::OFF_PHIQ, 4096, 256, LAYOUT_SW32);
+                    for (int i = 0; ok && i < n_lead; ++i) {
+                        const int ls = i % NLS;
+                        const bool alt = i & 1;
+                        if (!(ok = wait_bar(BAR(alt ? FB_PHIQ_FULL : FB_PHIK_FULL), (alt ? qn : upd_idx) & 1,
+                                            abort_flag, alt ? SITE_PHIQ_FULL : SITE_PHIK_FULL)))
+                            break;
+                        tc_fence_after();
+                        const uint64_t d_va = smem_desc(sb + CF::lead_v(ls), CF::OFF_LONES - CF::lead_v(ls), 1024,
+                                                        LAYOUT_SW128);
+                        const uint64_t d_f = alt ? d_phiq_k : d_phik;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            mma_ss(t_s, v_step<CF::ZROW>(d_va, j), dadd(d_f, 512 * j), ID_UPD,
+                                   (i > 0 || j > 0) ? 1u : 0u);
+                        mma_commit(BAR(alt ? FB_PHIQ_FREE : FB_PHIK_FREE));
+                        mma_commit(BAR(FB_LFREE0 + ls));  // UPD read v_c (f(k) is built)
+                        BASED_TRACE_EV(i, TE_LEAD_UPD);
+                        if (alt) ++qn;
+                        else ++upd_idx;
+                    }
+                    if (ok && n_lead > 0) mma_commit(BAR(FB_UPD_DONE));
+                }
                 for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
-                    const int s = n % CF::NST;
+                    const int s = stage_of(n);
                     const int ob = FAST ? (n & 1) : 0;
                     const uint64_t d_va = s == 0 ? d_va0 : (s == 1 ? d_va1 : d_va2);
                     const uint32_t t_out = ob ? t_o1 : t_o0;
@@ -1095,7 +1271,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int t = (warp - 8) * 32 + lane;  // token of the chunk = TMEM lane = output row
         const int q4 = warp & 3;
         const uint32_t lo = static_cast<uint32_t>(q4 * 32) << 16;
-        int ro_idx = 0, upd_idx = 0;
+        int qn = 0, upd_idx = 0;  // fills of the f~(q) and the f(k) tile
         bool ok = true;
 
         // Output tile: o = O_num / (O_den + 1e-6), written through staging buffers as pieces of
@@ -1184,8 +1360,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             return true;
         };
         auto build_q = [&](int n, int s) -> bool {
-            if (ro_idx > 0 &&
-                !wait_bar(BAR(FB_PHIQ_FREE), (ro_idx - 1) & 1, abort_flag, SITE_PHIQ_FREE))
+            if (qn > 0 && !wait_bar(BAR(FB_PHIQ_FREE), (qn - 1) & 1, abort_flag, SITE_PHIQ_FREE))
                 return false;
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_BEGIN);
             build_features<K>(sb + CF::OFF_RAWQ + s * CF::RAW, sb + CF::OFF_PHIQ, t, kBf16Half2, 0, CF::NBLK);
@@ -1193,7 +1368,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(FB_PHIQ_FULL));
             if (warp == 8 && lane == 0) BASED_TRACE_EV(n, TE_PHIQ_END);
-            ++ro_idx;
+            ++qn;
             return true;
         };
         auto build_k = [&](int n, int s) -> bool {
@@ -1209,15 +1384,36 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ++upd_idx;
             return true;
         };
+        if constexpr (LEADIN) {
+            // lead-in: f(k) of the head's chunks before the range, alternately into the f(k) and
+            // the f~(q) tile
+            for (int i = 0; ok && i < n_lead; ++i) {
+                const int ls = i % NLS;
+                if (!(ok = wait_bar(BAR(FB_LFULL0 + ls), (i / NLS) & 1, abort_flag, SITE_TMA_FULL))) break;
+                const bool alt = i & 1;
+                const int fill = alt ? qn : upd_idx;
+                if (fill > 0 && !(ok = wait_bar(BAR(alt ? FB_PHIQ_FREE : FB_PHIK_FREE), (fill - 1) & 1, abort_flag,
+                                                alt ? SITE_PHIQ_FREE : SITE_PHIK_FREE)))
+                    break;
+                if (warp == 8 && lane == 0) BASED_TRACE_EV(i, TE_LEAD_BUILD0);
+                build_features<K>(sb + CF::lead_k(ls), sb + (alt ? CF::OFF_PHIQ : CF::OFF_PHIK), t, kBf16One2, 0,
+                                  CF::NBLK);
+                if (warp == 8 && lane == 0) BASED_TRACE_EV(i, TE_LEAD_BUILD1);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(alt ? FB_PHIQ_FULL : FB_PHIK_FULL));
+                if (alt) ++qn;
+                else ++upd_idx;
+            }
+        }
         Cursor cu;
         cu.init(g0, nchunks, n_c, Hl, L, r_lane);
         int pb = 0, ph = 0, pt0 = 0;  // coordinates of the previous chunk (for its epilogue)
         for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
-            const int s = n % CF::NST;
+            const int s = stage_of(n);
             if (!FAST && n > 0 && !(ok = epilogue(n - 1, pb, ph, pt0))) break;
             if (cu.has_ro() || cu.has_upd()) {
-                if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s), (n / CF::NST) & 1, abort_flag,
-                                    SITE_TMA_FULL)))
+                if (!(ok = wait_bar(BAR(FB_TMA_FULL0 + s), stage_par(n), abort_flag, SITE_TMA_FULL)))
                     break;
                 if (FAST) {  // the state update comes first in the MMA order
                     if (cu.has_upd() && !(ok = build_k(n, s))) break;
@@ -1353,11 +1549,11 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         int cidx = 0;
         // A range that starts inside a head continues from the prefix state of the chunks before
         // it: load it into TMEM, then convert it like any other state.
-        if (pre.cnt[j_range] > 0) {
+        if (!LEADIN && rg.cnt[j_range] > 0) {
             // The prefix is the sum of the partial states of the pieces of the head before this
-            // range: slots pre.slot .. pre.slot + m - 1 (m <= kMaxChain; m = 1 when a scan has
+            // range: slots slot .. slot + m - 1 (m <= kMaxChain; m = 1 when a scan has
             // already summed them).
-            const int m = pre.cnt[j_range];
+            const int m = rg.cnt[j_range];
             // launched as a dependent of the aggregate / scan kernel: only this read of their
             // output waits for them (every other role starts right away)
             griddep_wait();
@@ -1366,7 +1562,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 63) * 32 + 24] = global_timer_ns();
 #endif
             const float *slot =
-                prefix + (static_cast<size_t>(pre.slot[j_range]) + static_cast<size_t>(r_lane) * lane_slots) * CF::SLOT;
+                prefix + (static_cast<size_t>(rg.slot[j_range]) + static_cast<size_t>(r_lane) * lane_slots) * CF::SLOT;
             // One code path per chain length, so that every load it issues is needed and all of a
             // step's loads are in flight together; the terms are summed in range order.
             auto load_prefix = [&](auto chain_len) {
@@ -1415,9 +1611,29 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             convert(cidx++, 63);
         }
         int u = 0;
+        bool ok = true;
+        if (LEADIN && n_lead > 0) {
+            // the state summed by the lead-in: one UPD_DONE phase for all of its chunks
+            ok = wait_bar(BAR(FB_UPD_DONE), 0, abort_flag, SITE_UPD_DONE);
+            if (ok) {
+                tc_fence_after();
+                if constexpr (kLeadOverSbf) {
+                    // lead-in stages were over the state operands: rows V + 2 .. of both are
+                    // zeroed again (the lead-in's reads of them are complete)
+                    constexpr int kPad = (CF::SBF_ROWS - V - 2) * 2;  // 16-byte pieces per block
+                    for (int i = static_cast<int>(threadIdx.x) - 12 * 32; i < CF::NSBF * CF::NBLK * kPad; i += 3 * 32)
+                        st_shared_v4(sb + CF::OFF_SBF + CF::SBF_BLK * (i / kPad) + (V + 2) * 32 + 16 * (i % kPad), 0u,
+                                     0u, 0u, 0u);
+                    // (each warp's proxy fence in the conversion covers these stores before its
+                    // SBF_FULL arrival)
+                }
+                ok = convert(cidx++, 63);
+            }
+            u = 1;
+        }
         Cursor cu;
         cu.init(g0, nchunks, n_c, Hl, L, r_lane);
-        for (int n = 0; n < nchunks; ++n, cu.next()) {
+        for (int n = 0; ok && n < nchunks; ++n, cu.next()) {
             if (!cu.has_upd()) continue;
             if (!wait_bar(BAR(FB_UPD_DONE), u & 1, abort_flag, SITE_UPD_DONE)) break;
             tc_fence_after();

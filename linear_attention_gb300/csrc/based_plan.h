@@ -24,4 +24,41 @@ inline LaneSplit lane_split(int B, int T, int H, int K, int sms) {
     return s;
 }
 
+// Estimated makespan, in the units of the lead-in cost model (thousandths of a forward chunk), of
+// the other way to give ranges their prefixes: the aggregate pass (its longest CTA load in
+// chunks: agg_load), the scan when the plan needs it, the prefix loads, then the longest range of
+// the even cut. Fitted to calls measured on GB300 (V = 64): about 6.8 forward chunks of fixed
+// cost (launch, the aggregate pass's fill and slot writes, the prefix load and conversion) and
+// 0.29 per chunk of the longest aggregate load.
+constexpr long long kAggFixedCost = 6800, kAggChunkCost = 290, kScanCost = 1600;
+inline long long slot_plan_cost(long long N, int G, long long agg_load, bool scan) {
+    return kStartCost + kAggFixedCost + kAggChunkCost * agg_load + (scan ? kScanCost : 0) + 1000 * ((N + G - 1) / G);
+}
+
+// Lead-ins or slots (V = 64, when some range of the even cut needs a prefix): the lead-in cut of
+// the lane's chunks is written to R, and it is taken when the slot plan's estimate (agg: the
+// aggregate plan of the even cut) exceeds its own by kLeadMargin percent. The estimates are of
+// single calls; calls issued back to back cost the lead-in plan more (every CTA of the next call
+// starts its loads only when the last one of this call ends, while the slot plan's aggregate
+// pass overlaps that tail). Measured on GB300 (us per call, back to back, slots / lead-ins, with
+// the estimates' ratio): B2 T2048 H16 K16 23.9 / 18.9 (1.55), B1 T512 H2 K8 7.5 / 6.1 (1.73),
+// B4 T4096 H16 K16 48.7 / 45.1 (1.27), B8 T16384 H32 K16 467 / 481 (1.03).
+// Returns the number of ranges of the lead-in cut (the rest are empty), or 0 when the slot plan
+// stays.
+constexpr long long kLeadMargin = 15;
+inline int choose_lead_in(long long N, int G, int n_c, int V, const AggPlan &agg, Ranges &R) {
+    if (V != 64) return 0;
+    const long long cost_lead = lead_cut(N, G, n_c, R);
+    long long agg_load = 0;
+    for (int j = 0; j < agg.pieces.n_cta; ++j) {
+        long long load = 0;
+        for (int q = agg.pieces.cta_first[j]; q < agg.pieces.cta_first[j + 1]; ++q) load += agg.pieces.len[q];
+        agg_load = load > agg_load ? load : agg_load;
+    }
+    if (100 * slot_plan_cost(N, G, agg_load, agg.scan) < (100 + kLeadMargin) * cost_lead) return 0;
+    int used = 0;
+    while (used < G && R.g0[used + 1] > R.g0[used]) ++used;
+    return used;
+}
+
 }  // namespace based

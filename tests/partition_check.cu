@@ -9,7 +9,11 @@
 //    fallback);
 //  - every range that starts inside a head finds in the slots it reads (after the scan, when the
 //    plan runs one) exactly the chunks of its head before its first chunk, and no slot is read that
-//    the aggregate pass did not write.
+//    the aggregate pass did not write;
+//  - the lead-in cut: its ranges, walked with the cursor from the start of each one's lead-in,
+//    cover every (b, h, chunk) exactly once outside the lead-ins, each lead-in is the chunks of
+//    its range's first head before the range, and no range is longer than the cost model allows
+//    (the makespan it returns).
 #include <cstdio>
 #include <vector>
 
@@ -19,6 +23,7 @@ using namespace based;
 
 namespace {
 AggPlan plan;  // large: kept out of the stack
+Ranges lead;
 
 // Every (b, h, c) is visited once by the CTAs' cursors.
 bool lanes_cover(int B, int H, int n_c, int L, long long N, int G) {
@@ -39,10 +44,45 @@ bool lanes_cover(int B, int H, int n_c, int L, long long N, int G) {
         if (!s) return false;
     return true;
 }
+
+// The lead-in cut R (G ranges, the first `used` non-empty, makespan M): every (b, h, c) is in
+// exactly one range, every lead-in is [head start, g0) of the range's first head, and every
+// range's cost is at most M.
+bool lead_cover(int B, int H, int n_c, int L, long long N, int G, const Ranges &R, int used, long long M) {
+    if (used < 1 || used > G || R.g0[0] != 0 || R.g0[used] != N) return false;
+    for (int j = used; j <= G; ++j)
+        if (R.g0[j] != N) return false;
+    std::vector<unsigned char> seen(static_cast<size_t>(B) * H * n_c, 0);
+    for (int x = 0; x < used * L; ++x) {
+        const int j = x / L, r = x % L;
+        const long long g0 = R.g0[j], g1 = R.g0[j + 1];
+        const int lead_n = static_cast<int>(g0 % n_c);
+        if (g1 <= g0 || !R.lead_in || R.cnt[j] != 0) return false;
+        if (range_cost(lead_n, g1 - g0) > M) return false;
+        Cursor cu;
+        cu.init(g0 - lead_n, static_cast<int>(lead_n + g1 - g0), n_c, H / L, L, r);
+        const int b0 = cu.b, h0 = cu.h;
+        if (cu.c != 0 && lead_n > 0) return false;
+        for (long long g = g0 - lead_n; g < g1; ++g, cu.next()) {
+            if (cu.b < 0 || cu.b >= B || cu.h < 0 || cu.h >= H || cu.h % L != r) return false;
+            if (g < g0) {  // lead-in: the first head, chunks 0 .. lead_n - 1
+                if (cu.b != b0 || cu.h != h0 || cu.c != g - (g0 - lead_n)) return false;
+                continue;
+            }
+            unsigned char &s = seen[(static_cast<size_t>(cu.b) * H + cu.h) * n_c + cu.c];
+            if (s) return false;
+            s = 1;
+        }
+    }
+    for (unsigned char s : seen)
+        if (!s) return false;
+    return true;
+}
 }  // namespace
 
 int main() {
-    long long checked = 0, balanced_plans = 0, fallback_plans = 0, scanned = 0, laned = 0;
+    long long checked = 0, balanced_plans = 0, fallback_plans = 0, scanned = 0, laned = 0, lead_cuts = 0,
+              lead_chosen = 0;
     for (int sms : {1, 2, 7, 148, 152, 160, 256}) {
         for (int K : {8, 16}) {
             for (int B : {1, 3}) {
@@ -66,6 +106,16 @@ int main() {
                             return 1;
                         }
                         if (L > 1) ++laned;
+                        {
+                            const long long M = lead_cut(N, G, n_c, lead);
+                            int used = 0;
+                            while (used < G && lead.g0[used + 1] > lead.g0[used]) ++used;
+                            if (!lead_cover(B, H, n_c, L, N, G, lead, used, M)) {
+                                printf("lead-in cut: sms=%d K=%d B=%d H=%d T=%d L=%d\n", sms, K, B, H, T, L);
+                                return 1;
+                            }
+                            ++lead_cuts;
+                        }
                         for (int max_slots : {kMaxPieces, 203, 0}) {
                             std::vector<int> covered(N, 0), in_stretch(N, 0);
                             for (int i = 0; i < G; ++i) {
@@ -80,6 +130,20 @@ int main() {
                             for (long long g = 0; g < N; ++g)
                                 if (covered[g] != 1) { printf("chunk %lld covered %d times\n", g, covered[g]); return 1; }
                             make_agg_plan(N, G, n_c, G, max_slots, plan);
+                            {
+                                bool need = false;
+                                for (int i = 0; i < G; ++i) need = need || has_aggregate(N, G, i, n_c);
+                                Ranges chosen;
+                                const int used = need ? choose_lead_in(N, G, n_c, 64, plan, chosen) : 0;
+                                if (used > 0) {
+                                    ++lead_chosen;
+                                    if (!lead_cover(B, H, n_c, L, N, G, chosen, used, lead_cut(N, G, n_c, lead))) {
+                                        printf("chosen lead-in cut\n");
+                                        return 1;
+                                    }
+                                }
+                                if (choose_lead_in(N, G, n_c, 128, plan, chosen) != 0) { printf("lead-in for V = 128\n"); return 1; }
+                            }
                             const AggPieces &A = plan.pieces;
                             // pieces: inside one head and one stretch, each stretch chunk exactly once
                             std::vector<int> piece_cov(N, 0);
@@ -153,7 +217,7 @@ int main() {
         }
     }
     printf("ok %lld prefixed ranges checked (%lld balanced plans, %lld one-stretch-per-CTA, %lld with a scan, "
-           "%lld shapes with several head lanes)\n",
-           checked, balanced_plans, fallback_plans, scanned, laned);
+           "%lld shapes with several head lanes, %lld lead-in cuts, %lld plans choose lead-ins)\n",
+           checked, balanced_plans, fallback_plans, scanned, laned, lead_cuts, lead_chosen);
     return 0;
 }

@@ -78,16 +78,23 @@ def test_small_shapes_match_oracle(B, T, H, K, V, seed, scale, cuda_device):
     _assert_close(o, ref, (B, T, H, K, V))
 
 
-# Both prefix paths, with the kernel count they launch on a 152-SM GB300: the forward kernel sums
-# up to four partial states into a prefix itself (aggregate + forward); longer chains of partial
-# states are summed by the scan kernel first (aggregate + scan + forward).
+# The three ways a range that starts inside a head gets its prefix, with the kernel count they
+# launch on a 152-SM GB300: the forward kernel sums up to four partial states itself (aggregate +
+# forward); longer chains of partial states are summed by the scan kernel first (aggregate +
+# scan + forward); or (V = 64, where the cost model prefers it) each CTA runs a lead-in, the state
+# update alone over its head's chunks before its range (forward kernel alone).
 PREFIX_PATHS = [
     # B, T, H, K, V, seed, kernels
     (1, 1024, 32, 16, 128, 50, 2),  # prefixes of up to four slots
-    (2, 1024, 16, 16, 64, 51, 2),   # prefixes of up to four slots
     (1, 512, 32, 8, 128, 52, 2),    # up to three slots, eight head lanes
     (1, 2048, 4, 16, 128, 53, 3),   # one head per lane cut into many ranges: scan
-    (1, 2048, 8, 8, 64, 54, 3),
+    (1, 8192, 8, 16, 64, 51, 3),    # V = 64 with long heads: slots and the scan
+    (1, 2048, 8, 8, 64, 54, 1),     # lead-ins of up to 15 chunks, eight head lanes
+    (2, 1024, 16, 16, 64, 55, 1),   # lead-ins of up to 7 chunks
+    (1, 257, 2, 16, 64, 56, 1),     # a two-chunk lead-in into a ragged last chunk
+    (1, 3000, 16, 8, 64, 57, 1),    # lead-ins of up to 23 chunks, ragged tail
+    (2, 4096, 8, 8, 64, 58, 1),     # lead-ins of up to 31 chunks (the stages wrap many times)
+    (3, 1100, 12, 16, 64, 59, 1),   # ranges across head boundaries
 ]
 
 
@@ -256,7 +263,7 @@ sys.path.insert(0, sys.argv[1])
 from linear_attention_gb300.based import based_fwd, workspace_size
 from linear_attention_gb300.inputs import make_inputs
 dev = torch.device("cuda:0")
-small, big = (2, 1500, 3, 16, 128, 60), (4, 4096, 16, 16, 64, 61)
+small, big = (2, 1500, 3, 16, 128, 60), (2, 4096, 16, 16, 128, 61)
 assert workspace_size(*big[:5]) > workspace_size(*small[:5]) > 0
 q, k, v = [t.to(dev) for t in make_inputs(*small)]
 ref = based_fwd(q, k, v)  # first call on the device: sizes the library workspace for `small`
