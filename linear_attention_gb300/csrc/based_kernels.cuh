@@ -1643,8 +1643,10 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 
     // ---- teardown ------------------------------------------------------------------------------
+    // (every thread must be done with TMEM before it is released: the single-lane roles reach
+    // this barrier after the other lanes of their warps, so it counts threads, not warps)
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -1994,7 +1996,7 @@ based_agg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         trace_buf_[(static_cast<size_t>(blockIdx.x) * 64 + 40) * 32 + 9] = global_timer_ns();
 #endif
     tc_fence_before();
-    __syncthreads();
+    cta_sync();
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);

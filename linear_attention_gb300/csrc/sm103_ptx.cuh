@@ -118,6 +118,12 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 __device__ __forceinline__ void bulk_wait_group_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Barrier 0 over all threads of the CTA, counted per thread (barrier.sync without .aligned): the
+// form for code where the threads of a warp reach it at different times (roles run by one lane
+// of a warp while the other lanes go ahead). The aligned form (__syncthreads, bar.sync) is
+// undefined there and was seen (by stage timestamps) to complete before every thread arrived;
+// after a structured branch, which the compiler reconverges, it is exact and costs less.
+__device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
 // Named barrier among `count` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
