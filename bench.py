@@ -327,7 +327,7 @@ def run_gpu(args, w, world, rank, local):
     clk = clocks.stop() if clocks is not None else None
     elapsed_ms = t_start.elapsed_time(t_stop)
     # the forward kernel alone: K more steps with CUDA events recorded on the launch stream right
-    # around it (this launches it without overlap with the aggregate pass, so its duration is
+    # around it (this launches it without overlap with the kernel before it, so its duration is
     # not shortened by early start)
     torch.cuda.synchronize(dev)
     for j in range(args.steps):
@@ -384,8 +384,10 @@ def run_gpu(args, w, world, rank, local):
             "l2": f"{nsets} rotating input/output sets ({nsets * wbytes / 2**20:.0f} MiB > 3x L2)",
             "output": "bf16" if obf else "fp32",
             "launch": f"stream launches, one {'based_fwd_bf16_out' if obf else 'based_fwd'} call per step "
-                      f"({launches} kernel(s): aggregate, scan when a prefix chains more than four "
-                      "partial states, forward; the later ones as programmatic dependents)"}),
+                      f"({launches} kernel(s): the forward kernel alone when the ranges that start "
+                      "inside a head run lead-ins; else aggregate, scan when a prefix chains more "
+                      "than four partial states, forward, the later ones as programmatic "
+                      "dependents)"}),
         "tflops": flops / (ms_per_step * 1e-3) / 1e12,
         "pct_bf16_peak": 100.0 * flops / (ms_per_step * 1e-3) / (tc * 1e12),
         "pct_roofline_step": 100.0 * t_roof_ms / ms_per_step,
