@@ -84,6 +84,19 @@ def _check(rc: int, what: str):
         raise BasedError(f"{what} failed: {msg} ({rc})" + (f": {cuda}" if cuda else ""))
 
 
+def _on_device(dev: torch.device, fn, *args) -> int:
+    # fn(*args) with dev as the current CUDA device; the switch (a context manager, a few
+    # microseconds per call) only when it is not current already
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
+def _stream_ptr(dev: torch.device, stream: Optional[torch.cuda.Stream]) -> int:
+    return (stream if stream is not None else torch.cuda.current_stream(dev)).cuda_stream
+
+
 def _scale_arg(scale: Optional[float]) -> float:
     # None (or a non-positive value) lets the library use its default K ** -0.5
     return -1.0 if scale is None else float(scale)
@@ -118,15 +131,15 @@ def based_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional
         out = torch.empty(B, T, H, V, dtype=torch.float32, device=q.device)
     elif out.dtype != torch.float32 or tuple(out.shape) != (B, T, H, V) or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of shape (B,T,H,V)")
-    with torch.cuda.device(q.device):
-        st = stream if stream is not None else torch.cuda.current_stream(q.device)
-        if workspace is None:
-            rc = L.based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
-                             _scale_arg(scale), out.data_ptr(), st.cuda_stream)
-        else:
-            rc = L.based_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
-                                _scale_arg(scale), out.data_ptr(), workspace.data_ptr(),
-                                workspace.numel() * workspace.element_size(), st.cuda_stream)
+    dev = q.device
+    st = _stream_ptr(dev, stream)
+    if workspace is None:
+        rc = _on_device(dev, L.based_fwd, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                        _scale_arg(scale), out.data_ptr(), st)
+    else:
+        rc = _on_device(dev, L.based_fwd_ws, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                        _scale_arg(scale), out.data_ptr(), workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), st)
     _check(rc, "based_fwd")
     return out
 
@@ -149,11 +162,9 @@ def based_fwd_bf16_out(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale:
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (
         workspace.data_ptr(), workspace.numel() * workspace.element_size())
     eb, ee = (None, None) if events is None else (events[0].cuda_event, events[1].cuda_event)
-    with torch.cuda.device(q.device):
-        st = stream if stream is not None else torch.cuda.current_stream(q.device)
-        rc = L.based_fwd_bf16_out(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
-                                  _scale_arg(scale), out.data_ptr(), ws_ptr, ws_bytes,
-                                  st.cuda_stream, eb, ee)
+    dev = q.device
+    rc = _on_device(dev, L.based_fwd_bf16_out, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                    _scale_arg(scale), out.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(dev, stream), eb, ee)
     _check(rc, "based_fwd_bf16_out")
     return out
 
@@ -170,10 +181,9 @@ def based_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: to
         raise ValueError("based_fwd_noalloc takes CUDA tensors")
     if out.dtype != torch.float32 or tuple(out.shape) != (B, T, H, V) or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of shape (B,T,H,V)")
-    with torch.cuda.device(q.device):
-        st = stream if stream is not None else torch.cuda.current_stream(q.device)
-        rc = L.based_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
-                                 _scale_arg(scale), out.data_ptr(), st.cuda_stream)
+    dev = q.device
+    rc = _on_device(dev, L.based_fwd_noalloc, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                    _scale_arg(scale), out.data_ptr(), _stream_ptr(dev, stream))
     _check(rc, "based_fwd_noalloc")
     return out
 
@@ -186,11 +196,12 @@ def based_fwd_timed(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torc
     handles exist) on the stream right before and after the forward kernel."""
     L = _load()
     B, T, H, K, V = _shapes(q, k, v)
-    with torch.cuda.device(q.device):
-        st = stream if stream is not None else torch.cuda.current_stream(q.device)
-        rc = L.based_fwd_timed(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
-                               _scale_arg(scale), out.data_ptr(), st.cuda_stream,
-                               ev_begin.cuda_event, ev_end.cuda_event)
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and out.is_cuda):
+        raise ValueError("based_fwd_timed takes CUDA tensors")
+    dev = q.device
+    rc = _on_device(dev, L.based_fwd_timed, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, K, V,
+                    _scale_arg(scale), out.data_ptr(), _stream_ptr(dev, stream), ev_begin.cuda_event,
+                    ev_end.cuda_event)
     _check(rc, "based_fwd_timed")
     return out
 

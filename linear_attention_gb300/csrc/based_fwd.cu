@@ -141,7 +141,7 @@ int slot_floats(int K, int V) { return (V + 1) * ((K == 16) ? 160 : 48); }
 
 // max_ws: workspace bytes the plan may use at most (the balanced aggregate pass needs a slot per
 // piece, up to about twice the ranges; with less it falls back to one slot per range)
-Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~static_cast<size_t>(0)) {
+Plan build_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws) {
     Plan p;
     const LaneSplit ls = lane_split(B, T, H, K, sms);
     p.n_c = ls.n_c;
@@ -175,6 +175,32 @@ Plan make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~stat
     }
     p.ws_bytes = p.need_agg ? static_cast<size_t>(p.L) * p.agg.pieces.n * slot_bytes : 0;
     return p;
+}
+
+// The plan of a shape, from a per-thread cache of the last few shapes: a call repeats the shape
+// of the calls before it far more often than not, and building a plan (the aggregate plan, the
+// bisection of the lead-in cut) costs host time comparable to a small call's kernel time. The
+// reference stays valid until this thread's next make_plan call.
+const Plan &make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws = ~static_cast<size_t>(0)) {
+    struct Entry {
+        int key[6];
+        size_t max_ws;
+        bool used;
+        Plan plan;
+    };
+    constexpr int kEntries = 4;
+    static thread_local Entry cache[kEntries];
+    static thread_local int next = 0;
+    const int key[6] = {B, T, H, K, V, sms};
+    for (Entry &e : cache)
+        if (e.used && e.max_ws == max_ws && std::memcmp(e.key, key, sizeof(key)) == 0) return e.plan;
+    Entry &e = cache[next];
+    next = (next + 1) % kEntries;
+    e.plan = build_plan(B, T, H, K, V, sms, max_ws);
+    std::memcpy(e.key, key, sizeof(key));
+    e.max_ws = max_ws;
+    e.used = true;
+    return e.plan;
 }
 
 // The kernels index the slots with the plan's tables and check none of them on the device: the
@@ -329,7 +355,7 @@ int run(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int T, i
     int dev;
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
     DeviceState &d = g_dev[dev];
-    const Plan p = make_plan(B, T, H, K, V, d.sms, max_ws);
+    const Plan &p = make_plan(B, T, H, K, V, d.sms, max_ws);
     if (!plan_in_bounds(p)) {
         snprintf(tl_cuda_error, sizeof(tl_cuda_error), "internal error: work plan out of bounds");
         return BASED_ERR_BAD_ARGUMENT;
@@ -411,11 +437,11 @@ int based_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v, i
     int dev;
     if ((rc = current_device(&dev)) != BASED_OK) return rc;
     // the plan that fits the fixed scratch (one slot per range when balanced pieces do not fit)
-    const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms, BASED_NOALLOC_SCRATCH_BYTES);
-    if (p.ws_bytes > BASED_NOALLOC_SCRATCH_BYTES) return BASED_ERR_SCRATCH_LIMIT;
+    const size_t ws_need = make_plan(B, T, H, K, V, g_dev[dev].sms, BASED_NOALLOC_SCRATCH_BYTES).ws_bytes;
+    if (ws_need > BASED_NOALLOC_SCRATCH_BYTES) return BASED_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
-    if (p.ws_bytes > 0 && (rc = noalloc_scratch(dev, &scratch)) != BASED_OK) return rc;
-    return run(q, k, v, B, T, H, K, V, scale, o, false, scratch, p.ws_bytes, false, stream, nullptr,
+    if (ws_need > 0 && (rc = noalloc_scratch(dev, &scratch)) != BASED_OK) return rc;
+    return run(q, k, v, B, T, H, K, V, scale, o, false, scratch, ws_need, false, stream, nullptr,
                nullptr, BASED_NOALLOC_SCRATCH_BYTES);
 }
 
@@ -423,7 +449,7 @@ int based_fwd_kernel_count(int B, int T, int H, int K, int V) {
     if ((K != 8 && K != 16) || (V != 64 && V != 128) || B < 1 || T < 1 || H < 1) return 0;
     int dev;
     if (current_device(&dev) != BASED_OK) return 0;
-    const Plan p = make_plan(B, T, H, K, V, g_dev[dev].sms);
+    const Plan &p = make_plan(B, T, H, K, V, g_dev[dev].sms);
     return p.need_agg ? (p.agg.scan ? 3 : 2) : 1;
 }
 
