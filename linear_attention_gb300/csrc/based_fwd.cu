@@ -169,6 +169,7 @@ Plan build_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws) {
         for (int j = 0; j <= p.G; ++j) p.rg.g0[j] = static_cast<int32_t>(cta_range(p.N, p.G, j).g0);  // j = G: N
         p.rg.lead_in = 0;
         for (int j = 0; j < p.G; ++j) {
+            p.rg.order[j] = static_cast<uint16_t>(j);
             p.rg.slot[j] = p.agg.pre.slot[j];
             p.rg.cnt[j] = p.agg.pre.cnt[j];
         }
@@ -212,6 +213,13 @@ const Plan &make_plan(int B, int T, int H, int K, int V, int sms, size_t max_ws 
 bool plan_in_bounds(const Plan &p) {
     if (p.G < 1 || p.G > kMaxRanges || p.rg.g0[0] != 0 || p.rg.g0[p.G] != p.N) return false;
     if (p.rg.lead_in != (p.lead_in ? 1 : 0)) return false;
+    {
+        bool seen[kMaxRanges] = {};  // the launch order is a permutation of the ranges
+        for (int i = 0; i < p.G; ++i) {
+            if (p.rg.order[i] >= p.G || seen[p.rg.order[i]]) return false;
+            seen[p.rg.order[i]] = true;
+        }
+    }
     for (int j = 0; j < p.G; ++j) {
         if (p.rg.g0[j + 1] <= p.rg.g0[j]) return false;
         if (p.lead_in && p.rg.cnt[j] != 0) return false;

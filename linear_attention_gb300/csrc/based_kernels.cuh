@@ -668,6 +668,11 @@ struct Ranges {
     int32_t g0[kMaxRanges + 1];
     uint16_t slot[kMaxRanges];
     uint8_t cnt[kMaxRanges];
+    // launch order: CTA group i (blockIdx / L) takes range order[i]. The block scheduler hands
+    // out CTAs in index order, so the ranges that cost most go first: calls issued back to back
+    // start a call's CTAs on the SMs the previous call frees first, and those finish their
+    // set-up before that call has ended.
+    uint16_t order[kMaxRanges];
     int32_t lead_in;
 };
 
@@ -716,6 +721,18 @@ inline long long lead_cut(long long N, int G, int n_c, Ranges &R) {
     for (int j = 0; j < G; ++j) {
         R.slot[j] = 0;
         R.cnt[j] = 0;
+        R.order[j] = static_cast<uint16_t>(j);
+    }
+    // the non-empty ranges by cost, highest first (insertion sort: G <= 256); ties keep their order
+    auto cost = [&](int j) { return range_cost(R.g0[j] % n_c, R.g0[j + 1] - R.g0[j]); };
+    int used = 0;
+    while (used < G && R.g0[used + 1] > R.g0[used]) ++used;
+    for (int a = 1; a < used; ++a) {
+        const uint16_t x = R.order[a];
+        const long long cx = cost(x);
+        int b = a;
+        for (; b > 0 && cost(R.order[b - 1]) < cx; --b) R.order[b] = R.order[b - 1];
+        R.order[b] = x;
     }
     return hi;
 }
@@ -801,7 +818,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto sbf_full_par = [&](int k) -> uint32_t { return static_cast<uint32_t>(CF::NSBF == 2 ? (k >> 1) & 1 : k & 1); };
 
     // range j of head lane r (N, G: chunks and ranges of one lane; lane_slots: slots per lane)
-    const int j_range = static_cast<int>(blockIdx.x) / L, r_lane = static_cast<int>(blockIdx.x) % L;
+    const int j_range = rg.order[static_cast<int>(blockIdx.x) / L], r_lane = static_cast<int>(blockIdx.x) % L;
     const int Hl = H / L;
     const long long g0 = rg.g0[j_range], g1 = rg.g0[j_range + 1];
     const int nchunks = static_cast<int>(g1 - g0);

@@ -12,8 +12,9 @@
 //    the aggregate pass did not write;
 //  - the lead-in cut: its ranges, walked with the cursor from the start of each one's lead-in,
 //    cover every (b, h, chunk) exactly once outside the lead-ins, each lead-in is the chunks of
-//    its range's first head before the range, and no range is longer than the cost model allows
-//    (the makespan it returns).
+//    its range's first head before the range, no range is longer than the cost model allows
+//    (the makespan it returns), and the launch order is a permutation of the ranges, costliest
+//    first.
 #include <cstdio>
 #include <vector>
 
@@ -76,6 +77,17 @@ bool lead_cover(int B, int H, int n_c, int L, long long N, int G, const Ranges &
     }
     for (unsigned char s : seen)
         if (!s) return false;
+    // the launch order: a permutation of the ranges, costliest first
+    std::vector<unsigned char> ord(used, 0);
+    for (int i = 0; i < used; ++i) {
+        if (R.order[i] >= used || ord[R.order[i]]) return false;
+        ord[R.order[i]] = 1;
+        if (i > 0) {
+            const int a = R.order[i - 1], b = R.order[i];
+            if (range_cost(R.g0[a] % n_c, R.g0[a + 1] - R.g0[a]) < range_cost(R.g0[b] % n_c, R.g0[b + 1] - R.g0[b]))
+                return false;
+        }
+    }
     return true;
 }
 }  // namespace
