@@ -677,11 +677,14 @@ struct Ranges {
 };
 
 // Cost model of a CTA, in thousandths of the time of one chunk of the forward pipeline (fitted to
-// stage traces of whole calls on GB300, V = 64, K = 16; one chunk is about 1.77 us):
+// stage traces of single calls on GB300, V = 64, K = 16; one chunk is about 1.77 us):
 // kStartCost for its start and end (set-up, the first loads, the pipeline's fill and drain),
 // kLeadStart more when it has a lead-in, kLeadCost per lead-in chunk (the f(k) tile and the state
-// update alone), 1000 per chunk of its range.
-constexpr long long kStartCost = 4950, kLeadStart = 815, kLeadCost = 252;
+// update alone), 1000 per chunk of its range. The traces give 252 per lead-in chunk; calls issued
+// back to back run lead-ins slower (more memory traffic at every call's start), and the cut with
+// 325 measured fastest there (B4 T4096 H16 41.5 us per call against 44.2 with 252, 42.1 with
+// 350, 46.0 with 220).
+constexpr long long kStartCost = 4950, kLeadStart = 815, kLeadCost = 325;
 __host__ __device__ inline long long range_cost(long long lead, long long len) {
     return kStartCost + (lead > 0 ? kLeadStart + lead * kLeadCost : 0) + 1000 * len;
 }

@@ -93,7 +93,8 @@ PREFIX_PATHS = [
     (2, 1024, 16, 16, 64, 55, 1),   # lead-ins of up to 7 chunks
     (1, 257, 2, 16, 64, 56, 1),     # a two-chunk lead-in into a ragged last chunk
     (1, 3000, 16, 8, 64, 57, 1),    # lead-ins of up to 23 chunks, ragged tail
-    (2, 4096, 8, 8, 64, 58, 1),     # lead-ins of up to 31 chunks (the stages wrap many times)
+    (2, 4096, 8, 8, 64, 58, 3),     # V = 64 with slots and the scan: the lead-in plan's estimate
+                                    # is within the margin
     (3, 1100, 12, 16, 64, 59, 1),   # ranges across head boundaries
 ]
 
