@@ -831,6 +831,7 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // range into stage n % NST.
     const int n_lead = LEADIN ? static_cast<int>(g0 % n_c) : 0;
     constexpr int NLS = CF::NLS > 0 ? CF::NLS : 1;
+    constexpr int kLeadAhead = 3;  // lead-in chunks prefetched into L2 ahead of the newest load
     constexpr bool kLeadOverSbf = LEADIN && K == 16;  // lead-in stages over the state operands
     auto stage_of = [&](int n) -> int { return n % CF::NST; };
     auto stage_par = [&](int n) -> uint32_t { return static_cast<uint32_t>((n / CF::NST) & 1); };
@@ -889,13 +890,13 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // wait for that kernel. After an aggregate pass the previous call has already completed.
         if (wait_prev) griddep_wait();
         if (LEADIN && n_lead > 0) {
-            // the lead-in's first loads, then the next NLS lead-in chunks into L2 (each later load
-            // prefetches the chunk NLS after it), so that the lead-in's loads wait on L2 rather
-            // than DRAM
+            // the lead-in's first loads, then the next kLeadAhead lead-in chunks into L2 (each later
+            // load prefetches the chunk kLeadAhead after it), so that the lead-in's loads wait on
+            // L2 rather than DRAM
             Cursor cl;
             cl.init(g0 - n_lead, n_lead, n_c, Hl, L, r_lane);
             for (int i = 0; i < n_lead_early; ++i, cl.next()) issue_lead(i, cl);
-            for (int i = n_lead_early; i < n_lead && i < 2 * NLS; ++i, cl.next()) {
+            for (int i = n_lead_early; i < n_lead && i < NLS + kLeadAhead; ++i, cl.next()) {
                 tma_prefetch_4d(&tm_k, 0, cl.h, cl.t0(), cl.b);
                 tma_prefetch_4d(&tm_v, 0, cl.h, cl.t0(), cl.b);
             }
@@ -945,18 +946,18 @@ based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int lead_issued = n_lead_early, issued = n_early;
             bool ok = true;
             if (LEADIN && n_lead > n_lead_early) {
-                Cursor cl, cp;  // cp: NLS chunks ahead (L2 prefetch)
+                Cursor cl, cp;  // cp: kLeadAhead chunks ahead (L2 prefetch)
                 cl.init(g0 - n_lead, n_lead, n_c, Hl, L, r_lane);
                 cp.init(g0 - n_lead, n_lead, n_c, Hl, L, r_lane);
                 for (int i = 0; i < n_lead_early; ++i) cl.next();
-                for (int i = 0; i < 2 * NLS; ++i) cp.next();
+                for (int i = 0; i < NLS + kLeadAhead; ++i) cp.next();
                 for (int i = n_lead_early; i < n_lead; ++i, cl.next()) {
                     const int ls = i % NLS;
                     if (!(ok = wait_bar(BAR(FB_LFREE0 + ls), ((i / NLS) - 1) & 1, abort_flag, SITE_STAGE_FREE)))
                         break;
                     issue_lead(i, cl);
                     ++lead_issued;
-                    if (i + NLS >= 2 * NLS && i + NLS < n_lead) {
+                    if (i + kLeadAhead < n_lead) {
                         tma_prefetch_4d(&tm_k, 0, cp.h, cp.t0(), cp.b);
                         tma_prefetch_4d(&tm_v, 0, cp.h, cp.t0(), cp.b);
                         cp.next();
