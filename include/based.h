@@ -27,7 +27,9 @@
  *
  * Ownership: the caller owns q, k, v, o. The library owns one workspace per device, which holds
  * per-segment partial states (fp32) for the chunk-parallel state scan; it lives until process
- * exit. The library allocates no device memory per call, with one exception: based_fwd (and
+ * exit. Shapes whose work plan gives the CTAs lead-ins instead (V = 64, where the plan finds that
+ * faster: each CTA that starts inside a head sums that head's earlier chunks itself) use no
+ * workspace (based_fwd_workspace_size() returns 0). The library allocates no device memory per call, with one exception: based_fwd (and
  * based_fwd_timed, and based_fwd_bf16_out with a NULL workspace) grow the library-owned
  * workspace with cudaMalloc when a shape needs more than any call before it. A workspace that a
  * larger one replaces is never freed, so that a CUDA graph which captured an earlier call still
@@ -163,7 +165,8 @@ BASED_API int based_fwd_timed(const uint16_t *q, const uint16_t *k, const uint16
                               void *ev_begin, void *ev_end);
 
 /* Number of kernels one based_fwd call launches for this shape on the current device: 1 (the
- * forward kernel alone), 2 (aggregate, forward: every prefix is the sum of at most four partial
+ * forward kernel alone: no CTA needs the state of chunks before its range, or the CTAs run
+ * lead-ins), 2 (aggregate, forward: every prefix is the sum of at most four partial
  * states, which the forward kernel adds itself) or 3 (aggregate, scan, forward: some prefix has
  * more); 0 for an unsupported shape. */
 BASED_API int based_fwd_kernel_count(int B, int T, int H, int K, int V);
