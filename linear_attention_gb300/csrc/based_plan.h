@@ -37,12 +37,11 @@ inline long long slot_plan_cost(long long N, int G, long long agg_load, bool sca
 
 // Lead-ins or slots (V = 64, when some range of the even cut needs a prefix): the lead-in cut of
 // the lane's chunks is written to R, and it is taken when the slot plan's estimate (agg: the
-// aggregate plan of the even cut) exceeds its own by kLeadMargin percent. The estimates are of
-// single calls; calls issued back to back cost the lead-in plan more (every CTA of the next call
-// starts its loads only when the last one of this call ends, while the slot plan's aggregate
-// pass overlaps that tail). Measured on GB300 (us per call, back to back, slots / lead-ins, with
-// the estimates' ratio): B2 T2048 H16 K16 23.9 / 18.9 (1.55), B1 T512 H2 K8 7.5 / 6.1 (1.73),
-// B4 T4096 H16 K16 48.7 / 45.1 (1.27), B8 T16384 H32 K16 467 / 481 (1.03).
+// aggregate plan of the even cut) exceeds its own by kLeadMargin percent: a margin for the two
+// estimates' errors (the slot plan's is a fit to measured calls, the lead-in plan's the per-CTA
+// cost model). Measured on GB300 (us per call, back to back, slots / lead-ins, with the
+// estimates' ratio): B2 T2048 H16 K16 23.9 / 17.9 (1.50), B1 T512 H2 K8 7.5 / 6.2 (1.68),
+// B4 T4096 H16 K16 48.6 / 41.5 (1.22), B8 T16384 H32 K16 467.3 / 471.3 (1.01).
 // Returns the number of ranges of the lead-in cut (the rest are empty), or 0 when the slot plan
 // stays.
 constexpr long long kLeadMargin = 15;
